@@ -1,0 +1,348 @@
+#!/usr/bin/env python3
+"""Benchmark of kdtv_verify_attn (tree-verify MLA-absorb attention).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl ours|reference] [--path tc|simt]
+
+One step = one kdtv_verify_attn call (absorb, tree-masked attention,
+split-KV combine, W_UV up-projection) on a seeded synthetic workload whose
+inputs are already resident in HBM; L2 is flushed (a 256 MiB write) before
+every timed call, outside the timed interval.  Prints ONE JSON line.
+
+The default workload is the Kimi-K2-shaped single request (64 heads,
+kv_lora 512, rope 64, prefix 4096, 64-node tree).  ``--impl reference`` times
+the fp64 CPU oracle on the same workload instead (bounded node sample per
+step, scaled to the whole call).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify MLA attn µs/call; HBM TB/s + TC TFLOP/s as % of roofline"
+UNIT = "us/call"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="kimi_single")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--path", default="tc", choices=["tc", "simt"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def work(wl):
+    """Algorithmic work of one call: visible-key FLOPs, latent-cache bytes,
+    all compulsory bytes."""
+    import numpy as np
+    from speculative_decoding_tree_mla_gb300 import workloads as W
+    s = wl.spec
+    f = wl.f32
+    attn = 0
+    for b in range(s.B):
+        depth = W.tree_depths(f["parent"][b])
+        attn += s.H * int((f["prefix_len"][b] + depth).sum()) * (
+            2 * (s.d_c + s.d_rope) + 2 * s.d_c)
+    absorb = 2 * s.B * s.N * s.H * s.d_nope * s.d_c
+    uproj = 2 * s.B * s.N * s.H * s.d_c * s.d_v
+    esz = 2 if s.dtype == "bf16" else 4
+    T = (np.asarray(f["prefix_len"]) + s.N).sum()
+    cache_bytes = int(T) * (s.d_c + s.d_rope) * esz
+    weights = s.H * s.d_c * (s.d_nope + s.d_v) * esz
+    q = s.B * s.N * s.H * (s.d_nope + s.d_rope) * esz
+    out = s.B * s.N * s.H * s.d_v * 4
+    return {"attn_flops": attn, "total_flops": attn + absorb + uproj,
+            "cache_bytes": cache_bytes, "all_bytes": cache_bytes + weights + q + out}
+
+
+class Clocks:
+    """nvidia-smi sampler run around the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}",
+                                       f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        mx = max(num(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(num(r[3]) for r in rows)}
+
+
+def dist_init(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allmax(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# -- the oracle on the host (reference arm and cpu_baseline leg) ---------------
+def oracle_time(wl, seconds, max_nodes=None):
+    """Times the oracle on a bounded node sample; returns (us per whole call,
+    sample description, threads)."""
+    import numpy as np
+    import oracle
+    f = wl.f32
+    s = wl.spec
+    nodes = [(b, i) for b in range(s.B) for i in range(s.N)]
+    rng = np.random.default_rng(0)
+    order = rng.permutation(len(nodes))
+    done = 0
+    t0 = time.perf_counter()
+    while (time.perf_counter() - t0 < seconds and done < len(nodes)
+           and (max_nodes is None or done < max_nodes)):
+        b, i = nodes[order[done]]
+        oracle.verify_attn_node(f["q_nope"], f["q_rope"], f["W_UK"], f["W_UV"], f["c_kv"],
+                                f["k_rope"], f["parent"], f["prefix_len"], b, i, s.scale,
+                                page_table=f.get("page_table"), page_size=wl.page_size)
+        done += 1
+    dt = time.perf_counter() - t0
+    us_call = dt / done * len(nodes) * 1e6
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS") or os.cpu_count() or 1)
+    return us_call, f"{done} of {len(nodes)} (request, node) pairs, random order", threads
+
+
+def run_reference(args, wl, rank, ws):
+    if rank != 0:
+        return
+    per_step = []
+    for k in range(args.warmup + args.steps):
+        us, sample, threads = oracle_time(wl, seconds=1e9, max_nodes=1)
+        if k >= args.warmup:
+            per_step.append(us)
+    v = statistics.mean(per_step)
+    cfg = config_dict(wl)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1000.0,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "each step: one random (request, node) pair of the "
+                                   "workload, scaled to all pairs"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def config_dict(wl):
+    s = wl.spec
+    f = wl.f32
+    return {"workload": s.name, "batch": s.B, "tree_nodes": s.N, "heads": s.H,
+            "d_nope": s.d_nope, "d_rope": s.d_rope, "d_v": s.d_v, "kv_lora": s.d_c,
+            "prefix_len_mean": float(sum(int(x) for x in f["prefix_len"]) / s.B),
+            "paged": s.paged, "seed": s.seed, "l2": "flushed (256 MiB write) before every call"}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+    import numpy as np  # noqa: F401
+    import torch
+    from speculative_decoding_tree_mla_gb300 import workloads as W
+    rank, ws, local = dist_init(args)
+    wl = W.make(args.config)
+    if args.impl == "reference":
+        run_reference(args, wl, rank, ws)
+        return
+
+    from speculative_decoding_tree_mla_gb300 import build, kdtv
+    if rank == 0:
+        build.build()
+    barrier(ws)
+    dev = torch.device("cuda", local)
+    flags = kdtv.KDTV_FLAG_SIMT if args.path == "simt" else 0
+    op = kdtv.for_workload(wl, dev, flags=flags)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    K, Wm = args.steps, max(3, args.warmup)
+
+    for _ in range(Wm):
+        flush.zero_()
+        op()
+    torch.cuda.synchronize()
+    if op.status() != 0:
+        raise SystemExit(f"device status {kdtv.STATUS[op.status()]}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    clocks = Clocks(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        op.set_phase_events(ev[k])
+        op()
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    op.set_phase_events(None)
+    st = op.status()
+    if st != 0:
+        raise SystemExit(f"device status {kdtv.STATUS[st]}")
+
+    call_ms = [e[0].elapsed_time(e[4]) for e in ev]
+    phase_ms = [[e[j].elapsed_time(e[j + 1]) for e in ev] for j in range(4)]
+    mean_ms = allmax(statistics.mean(call_ms), ws)
+    us_call = mean_ms * 1000.0 / ws        # whole job: ws replicas in parallel
+    wk = work(wl)
+    pk, pk_kind = peaks()
+    attn_ms = statistics.mean(phase_ms[1])
+    tflops = wk["attn_flops"] / (attn_ms * 1e-3) / 1e12
+    peak_tc = pk["bf16_tflops"]
+    roof_us = max(wk["cache_bytes"] / (pk["hbm_gbs"] * 1e9),
+                  wk["total_flops"] / (peak_tc * 1e12)) * 1e6
+    phases = {n: statistics.mean(x) * 1000.0 for n, x in
+              zip(["absorb_us", "attention_us", "combine_us", "up_proj_us"], phase_ms)}
+
+    # End to end: pinned host inputs -> device, call, result -> host.
+    names = ["q_nope", "q_rope", "W_UK", "W_UV", "c_kv", "k_rope", "parent", "prefix_len"]
+    if wl.page_size:
+        names.append("page_table")
+    host = {n: wl.t[n].contiguous().pin_memory() for n in names}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    out_host = torch.empty(op.out.shape, dtype=op.out.dtype).pin_memory()
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = []
+    K_e2e = min(K, 200)
+    for k in range(Wm + K_e2e):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for n in names:
+            op.t[n].copy_(host[n], non_blocking=True)
+        op()
+        out_host.copy_(op.out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if k >= Wm:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_us = allmax(statistics.mean(e2e_ms), ws) * 1000.0 / ws
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, sample, threads = oracle_time(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": ws, "steps": K,
+            "warmup": Wm, "ms_per_step": mean_ms, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.spec.dtype,
+            "data": "synthetic", "config": config_dict(wl),
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tc,
+                         "unit": "TFLOP/s", "frac": tflops / peak_tc, "traffic": None,
+                         "kernel": "attention (tree-masked scores, online softmax, P.c_kv)",
+                         "peak_source": f"{pk_kind} bf16_tflops (burst)"},
+            "call_roofline": {"t_roof_us": roof_us, "frac": roof_us / us_call,
+                              "tflops": wk["total_flops"] / (us_call * 1e-6) / 1e12,
+                              "cache_tbs": wk["cache_bytes"] / (us_call * 1e-6) / 1e12,
+                              "flops": wk["total_flops"], "cache_bytes": wk["cache_bytes"],
+                              "all_bytes": wk["all_bytes"]},
+            "phases": phases,
+            "p50_us": statistics.median(call_ms) * 1000.0,
+            "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": op.launches() * K,
+            "path": args.path,
+            "clocks": clk,
+            "wall_s_timed_region": t_wall,
+        }
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+// Host side of the C ABI declared in include/kdtv.h: argument validation, the
+// split-KV plan, workspace carving and dispatch to the CUDA-core or the
+// tensor-core path.  Allocates nothing.
+
+#include "kdtv_internal.cuh"
+
+#include <math.h>
+#include <string.h>
+
+namespace kdtv {
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices];
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices) g_sm_count[dev] = n;
+  return n;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_dims(const kdtv_dims* d) {
+  if (!d) return KDTV_ERR_INVALID_ARG;
+  if (d->B <= 0 || d->N <= 0 || d->H <= 0 || d->d_nope <= 0 || d->d_rope <= 0 ||
+      d->d_v <= 0 || d->d_c <= 0)
+    return KDTV_ERR_INVALID_ARG;
+  if (d->dtype != KDTV_F32 && d->dtype != KDTV_BF16) return KDTV_ERR_INVALID_ARG;
+  if (d->page_size < 0 || d->kv_chunk < 0) return KDTV_ERR_INVALID_ARG;
+  if (d->page_size == 0) {
+    if (d->t_stride < d->N) return KDTV_ERR_INVALID_ARG;
+  } else {
+    if (d->max_pages <= 0 || d->num_pages <= 0) return KDTV_ERR_INVALID_ARG;
+    if ((long long)d->max_pages * d->page_size > (1ll << 30)) return KDTV_ERR_INVALID_ARG;
+  }
+  if (d->N > kMaxNodes) return KDTV_ERR_UNSUPPORTED;
+  if (d->d_c > kMaxLatent || d->d_rope > kMaxRope || d->d_nope > 512 || d->d_v > 512)
+    return KDTV_ERR_UNSUPPORTED;
+  if ((long long)d->B * d->N * d->H > (1ll << 28)) return KDTV_ERR_UNSUPPORTED;
+  return KDTV_OK;
+}
+
+bool use_tensor_cores(const kdtv_dims* d) {
+  return d->dtype == KDTV_BF16 && !(d->flags & KDTV_FLAG_SIMT) && tc_supported(d);
+}
+
+int make_plan(const kdtv_dims* d, Plan* p) {
+  int st = check_dims(d);
+  if (st != KDTV_OK) return st;
+  if (d->dtype == KDTV_BF16 && !(d->flags & KDTV_FLAG_SIMT) && !tc_supported(d))
+    return KDTV_ERR_UNSUPPORTED;
+  memset(p, 0, sizeof(*p));
+  p->tensor_core = use_tensor_cores(d);
+  p->rows = d->B * d->N * d->H;
+  p->t_cap = d->page_size ? d->max_pages * d->page_size : d->t_stride;
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  int chunk;
+  if (p->tensor_core) {
+    chunk = tc_chunk(d, sms);
+  } else {
+    p->heads_per_cta = d->H < 16 ? d->H : 16;
+    long long base = (long long)d->B * d->N * ((d->H + p->heads_per_cta - 1) / p->heads_per_cta);
+    long long want = (2ll * sms + base - 1) / base;
+    long long max_s = (p->t_cap + 63) / 64;
+    if (want < 1) want = 1;
+    if (want > max_s) want = max_s;
+    chunk = (int)((p->t_cap + want - 1) / want);
+    chunk = (chunk + 31) / 32 * 32;
+  }
+  if (d->kv_chunk > 0) chunk = d->kv_chunk;
+  p->chunk = chunk;
+  p->splits = (p->t_cap + chunk - 1) / chunk;
+  if (p->splits > 1024) return KDTV_ERR_UNSUPPORTED;
+  const size_t rows = (size_t)p->rows;
+  size_t off = kStatusBytes;
+  p->off_qlat = off;    off = align256(off + rows * d->d_c * sizeof(float));
+  p->off_part_o = off;  off = align256(off + (size_t)p->splits * rows * d->d_c * sizeof(float));
+  p->off_part_ml = off; off = align256(off + (size_t)p->splits * rows * 2 * sizeof(float));
+  p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
+  p->total = off;
+  return KDTV_OK;
+}
+
+}  // namespace
+}  // namespace kdtv
+
+using namespace kdtv;
+
+extern "C" size_t kdtv_workspace_size(const kdtv_dims* d) {
+  Plan p;
+  if (make_plan(d, &p) != KDTV_OK) return 0;
+  return p.total;
+}
+
+extern "C" int kdtv_launches_per_call(const kdtv_dims* d) {
+  Plan p;
+  if (make_plan(d, &p) != KDTV_OK) return -1;
+  return p.tensor_core ? tc_launches(d) : 4;
+}
+
+extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const void* q_rope,
+                                const void* W_UK, const void* W_UV, const void* c_kv,
+                                const void* k_rope, const int32_t* parent,
+                                const int32_t* prefix_len, const int32_t* page_table,
+                                float* out, cudaStream_t stream) {
+  Plan p;
+  int st = make_plan(d, &p);
+  if (st != KDTV_OK) return st;
+  if (!q_nope || !q_rope || !W_UK || !W_UV || !c_kv || !k_rope || !parent || !prefix_len ||
+      !out)
+    return KDTV_ERR_INVALID_ARG;
+  if ((d->page_size > 0) != (page_table != nullptr)) return KDTV_ERR_INVALID_ARG;
+  if (!d->workspace || (reinterpret_cast<uintptr_t>(d->workspace) & 255u) ||
+      d->workspace_bytes < p.total)
+    return KDTV_ERR_INVALID_ARG;
+
+  Args a;
+  memset(&a, 0, sizeof(a));
+  a.B = d->B; a.N = d->N; a.H = d->H;
+  a.d_nope = d->d_nope; a.d_rope = d->d_rope; a.d_v = d->d_v; a.d_c = d->d_c;
+  a.dtype = d->dtype;
+  a.page_size = d->page_size; a.t_stride = d->t_stride;
+  a.max_pages = d->max_pages; a.num_pages = d->num_pages;
+  a.scale = d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)(d->d_nope + d->d_rope));
+  a.flags = d->flags;
+  a.chunk = p.chunk; a.splits = p.splits;
+  a.q_nope = q_nope; a.q_rope = q_rope; a.W_UK = W_UK; a.W_UV = W_UV;
+  a.c_kv = c_kv; a.k_rope = k_rope;
+  a.parent = parent; a.prefix_len = prefix_len; a.page_table = page_table;
+  a.out = out;
+  char* ws = static_cast<char*>(d->workspace);
+  a.status = reinterpret_cast<DeviceStatus*>(ws);
+  a.q_lat = ws + p.off_qlat;
+  a.part_o = reinterpret_cast<float*>(ws + p.off_part_o);
+  a.part_ml = reinterpret_cast<float*>(ws + p.off_part_ml);
+  a.o_lat = reinterpret_cast<float*>(ws + p.off_olat);
+
+  cudaEvent_t* ev = d->phase_events;
+  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return KDTV_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return KDTV_ERR_CUDA;
+  cudaError_t e = p.tensor_core ? launch_tc(a, p, stream, ev) : launch_simt(a, p, stream, ev);
+  return e == cudaSuccess ? KDTV_OK : KDTV_ERR_CUDA;
+}
+
+extern "C" int kdtv_get_device_status(const kdtv_dims* d, cudaStream_t stream) {
+  if (!d || !d->workspace) return KDTV_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return KDTV_ERR_CUDA;
+  unsigned int code = 0;
+  if (cudaMemcpy(&code, d->workspace, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KDTV_ERR_CUDA;
+  return (int)code;
+}
+
+extern "C" const char* kdtv_strerror(int s) {
+  switch (s) {
+    case KDTV_OK: return "KDTV_OK";
+    case KDTV_ERR_INVALID_ARG: return "KDTV_ERR_INVALID_ARG";
+    case KDTV_ERR_UNSUPPORTED: return "KDTV_ERR_UNSUPPORTED";
+    case KDTV_ERR_CUDA: return "KDTV_ERR_CUDA";
+    case KDTV_ERR_BAD_TREE: return "KDTV_ERR_BAD_TREE";
+    case KDTV_ERR_DEVICE_TIMEOUT: return "KDTV_ERR_DEVICE_TIMEOUT";
+    case KDTV_ERR_BAD_PREFIX: return "KDTV_ERR_BAD_PREFIX";
+    case KDTV_ERR_BAD_PAGE: return "KDTV_ERR_BAD_PAGE";
+    default: return "KDTV_ERR_UNKNOWN";
+  }
+}

@@ -1,0 +1,132 @@
+// Internal declarations shared by the CUDA translation units of libkdtv.
+// Nothing here is part of the public ABI (include/kdtv.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kdtv.h"
+
+namespace kdtv {
+
+constexpr int kMaxNodes = 128;        // ancestor masks are 4 x u32
+constexpr int kMaxLatent = 512;       // d_c bound on the fp32 path
+constexpr int kMaxRope = 64;
+constexpr int kStatusBytes = 256;
+
+// Status word layout at the start of the workspace.
+struct DeviceStatus {
+  unsigned int code;      // first kdtv_status recorded by any kernel (0 = OK)
+  unsigned int detail;    // kernel-specific detail of that first error
+  unsigned int abort;     // set with the code: lets other CTAs stop early
+  unsigned int pad[61];
+};
+
+__device__ __forceinline__ void record_error(DeviceStatus* st, unsigned int code,
+                                             unsigned int detail) {
+  if (atomicCAS(&st->code, 0u, code) == 0u) {
+    st->detail = detail;
+  }
+  atomicExch(&st->abort, 1u);
+}
+
+// Per-call plan: how the key range of each request is cut into split-KV
+// chunks and where each workspace region lives.  Computed identically by
+// kdtv_workspace_size and kdtv_verify_attn.
+struct Plan {
+  bool tensor_core;       // bf16 tcgen05 path
+  int rows;               // B * N * H query rows, row = (b * N + i) * H + h
+  int t_cap;              // max keys per request the cache layout can hold
+  int chunk;              // keys per split
+  int splits;             // splits per request (ceil(t_cap / chunk))
+  int heads_per_cta;      // SIMT attention: heads sharing one CTA
+  size_t off_qlat, off_part_o, off_part_ml, off_olat, total;
+};
+
+// Device-side view of the call (passed by value to kernels).
+struct Args {
+  int B, N, H, d_nope, d_rope, d_v, d_c;
+  int dtype;              // kdtv_dtype
+  int page_size, t_stride, max_pages, num_pages;
+  float scale;
+  unsigned int flags;
+  int chunk, splits;
+  const void* q_nope;
+  const void* q_rope;
+  const void* W_UK;
+  const void* W_UV;
+  const void* c_kv;
+  const void* k_rope;
+  const int32_t* parent;
+  const int32_t* prefix_len;
+  const int32_t* page_table;
+  float* out;
+  DeviceStatus* status;
+  void* q_lat;            // fp32 (SIMT) or bf16 (tensor core) [rows, d_c]
+  float* part_o;          // [splits, rows, d_c]
+  float* part_ml;         // [splits, rows, 2]  (running max m, sum l)
+  float* o_lat;           // [rows, d_c]
+};
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Row of logical position t of request b in a cache tensor with `width`
+// elements per row; -1 if the page id is out of range.
+__device__ __forceinline__ long long cache_row(const Args& a, int b, int t) {
+  if (a.page_size == 0) return (long long)b * a.t_stride + t;
+  int page = a.page_table[(long long)b * a.max_pages + t / a.page_size];
+  if (page < 0 || page >= a.num_pages) return -1;
+  return (long long)page * a.page_size + (t % a.page_size);
+}
+
+// Walks node i's root path, building its ancestor mask (bit a set for every a
+// on the path, i included).  Returns false, after recording BAD_TREE, if
+// parent[] is not a topologically ordered tree rooted at node 0.
+__device__ __forceinline__ bool ancestor_mask(const Args& a, int b, int i,
+                                              uint32_t mask[4]) {
+  const int32_t* par = a.parent + (long long)b * a.N;
+  mask[0] = mask[1] = mask[2] = mask[3] = 0u;
+  if (par[0] != -1) {
+    record_error(a.status, KDTV_ERR_BAD_TREE, (unsigned)b);
+    return false;
+  }
+  int j = i;
+  for (int step = 0; step <= a.N; ++step) {   // parent[j] < j bounds the walk
+    mask[j >> 5] |= 1u << (j & 31);
+    if (j == 0) return true;
+    int p = par[j];
+    if (p < 0 || p >= j) {
+      record_error(a.status, KDTV_ERR_BAD_TREE, (unsigned)(b * 65536 + j));
+      return false;
+    }
+    j = p;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool prefix_ok(const Args& a, int b, int* L) {
+  int l = a.prefix_len[b];
+  int cap = a.page_size ? a.max_pages * a.page_size : a.t_stride;
+  if (l < 0 || (long long)l + a.N > cap) {
+    record_error(a.status, KDTV_ERR_BAD_PREFIX, (unsigned)b);
+    return false;
+  }
+  *L = l;
+  return true;
+}
+
+// Launchers (one per translation unit).
+cudaError_t launch_simt(const Args& a, const Plan& p, cudaStream_t s,
+                        cudaEvent_t* ev);
+cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t s,
+                      cudaEvent_t* ev);
+cudaError_t launch_absorb(const Args& a, cudaStream_t s, bool bf16_out);
+cudaError_t launch_combine_uproj(const Args& a, const Plan& p, cudaStream_t s,
+                                 cudaEvent_t* ev);
+int tc_supported(const kdtv_dims* d);
+int tc_launches(const kdtv_dims* d);
+int tc_chunk(const kdtv_dims* d, int sm_count);
+
+}  // namespace kdtv

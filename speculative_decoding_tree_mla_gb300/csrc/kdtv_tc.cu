@@ -1,0 +1,528 @@
+// Tensor-core (tcgen05) path of kdtv_verify_attn: bf16 inputs, the MLA
+// latent layout d_c = 512, d_rope = 64, fp32 accumulation.
+//
+// The attention step (tree-masked scores, online softmax, P . c_kv) of the
+// "tree-verify MLA-absorb attention kernel with visibility masking" ("The
+// Moment of Proof: Validating a Native CUDA Speculative Decoding Engine",
+// section "The Context: Building a Native DDTree Engine from Scratch").
+//
+// Work decomposition.  A work item is (request b, tile of 128 query rows,
+// split-KV key range).  Query rows are (node, head) pairs with the head
+// fastest, so one tile holds 128/H nodes; every row of a node shares that
+// node's ancestor mask.  An item runs on a CLUSTER OF TWO CTAs that split
+// the latent dimension:
+//   CTA 0 holds q_lat[:, 0:256] + q_rope and the matching cache columns
+//         c_kv[:, 0:256] + k_rope;
+//   CTA 1 holds q_lat[:, 256:512] and c_kv[:, 256:512].
+// Each CTA computes a partial score tile S_c = Q_c K_c^T (tcgen05, TMEM),
+// the two partials are exchanged through distributed shared memory and
+// summed, both CTAs run the same online softmax on S = S_0 + S_1 (so they
+// agree bit for bit), and each accumulates its own half of the latent
+// output O_c += P . c_kv[:, 256c : 256c+256] in TMEM.  This keeps the 128-row
+// O accumulator at 256 TMEM columns per SM, next to two 64-column score
+// buffers, and the resident Q at 80 KB of shared memory per CTA.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs, warps 2-5 (one thread per query row / TMEM lane) do the
+// score exchange, masking, softmax, P stores and the epilogue.  Every wait is
+// bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL); on timeout the kernel
+// records KDTV_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs,
+// frees TMEM and returns.
+
+#include <cuda.h>
+
+#include "kdtv_internal.cuh"
+#include "kdtv_ptx.cuh"
+
+namespace kdtv {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128;          // query rows per tile (MMA M)
+constexpr int BN = 64;           // keys per tile (MMA N of Q.K^T)
+constexpr int CH = 64;           // bf16 columns per 128-byte swizzled chunk
+constexpr int kHalf = 256;       // latent columns per CTA
+constexpr int kStages = 2;
+constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk
+constexpr int kQChunk = BM * CH * 2;   // 16 KiB
+constexpr int kKVChunk = BN * CH * 2;  // 8 KiB
+constexpr int kRxStride = 68;    // floats per exchanged score row (64 + pad)
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kColO = 0;         // O_c: columns [0, 256)
+constexpr int kColS = 256;       // score buffers: [256, 320), [320, 384)
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = OFF_Q + kMaxCh * kQChunk;
+constexpr int OFF_P = OFF_KV + kStages * kMaxCh * kKVChunk;
+constexpr int OFF_RX = OFF_P + BM * CH * 2;
+constexpr int OFF_ANC = OFF_RX + BM * kRxStride * 4;
+constexpr int OFF_BAR = OFF_ANC + kMaxNodes * 16;
+constexpr int kNumBars = 16;
+constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
+constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
+
+enum Bar {
+  B_Q_FULL = 0, B_KV_FULL = 1, B_KV_EMPTY = 3, B_S_FULL = 5, B_S_EMPTY = 7,
+  B_P_FULL = 9, B_P_EMPTY = 10, B_O_FULL = 11, B_RX_FULL = 12, B_TX_OK = 13,
+  B_STALL = 14, B_MMA_DONE = 15
+};
+
+// Wait sites (reported as the timeout detail).
+enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_S_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK,
+            W_RX_FULL, W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN };
+
+struct TcCfg {
+  int row_tiles;               // ceil(N * H / 128)
+  unsigned long long limit_ns; // bound on every wait
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
+               const __grid_constant__ CUtensorMap tm_qrope,
+               const __grid_constant__ CUtensorMap tm_ckv,
+               const __grid_constant__ CUtensorMap tm_krope, const Args a, const TcCfg cfg) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t peer = rank ^ 1u;
+  const int item = blockIdx.x >> 1;
+  const int rt = item % cfg.row_tiles;
+  const int s = (item / cfg.row_tiles) % a.splits;
+  const int b = item / (cfg.row_tiles * a.splits);
+  const int nch = rank == 0 ? 5 : 4;
+  uint32_t* anc = reinterpret_cast<uint32_t*>(sm + OFF_ANC);
+  volatile int* misc = reinterpret_cast<volatile int*>(sm + OFF_MISC);
+  auto BAR = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
+  DeviceStatus* st = a.status;
+  const uint64_t limit = cfg.limit_ns;
+
+  // ---- prologue: barriers, validation, ancestor masks, TMEM ------------------------
+  if (tid == 0) {
+    mbar_init(BAR(B_Q_FULL), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(BAR(B_KV_FULL + i), 1);
+      mbar_init(BAR(B_KV_EMPTY + i), 1);
+      mbar_init(BAR(B_S_FULL + i), 1);
+      mbar_init(BAR(B_S_EMPTY + i), 128);
+    }
+    mbar_init(BAR(B_P_FULL), 128);
+    mbar_init(BAR(B_P_EMPTY), 1);
+    mbar_init(BAR(B_O_FULL), 1);
+    mbar_init(BAR(B_RX_FULL), 128);
+    mbar_init(BAR(B_TX_OK), 128);
+    mbar_init(BAR(B_STALL), 1);
+    mbar_init(BAR(B_MMA_DONE), 1);
+    fence_mbar_init();
+    int L = 0;
+    int ok = prefix_ok(a, b, &L) ? 1 : 0;
+    if (ok && a.page_size) {
+      const int T = L + a.N;
+      const int k0 = s * a.chunk, k1 = min(T, k0 + a.chunk);
+      for (int p = k0 / a.page_size; k0 < k1 && p <= (k1 - 1) / a.page_size; ++p) {
+        int page = a.page_table[(long long)b * a.max_pages + p];
+        if (page < 0 || page >= a.num_pages) {
+          record_error(st, KDTV_ERR_BAD_PAGE, (unsigned)b);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    misc[1] = ok;
+    misc[2] = L;
+    misc[3] = 1;   // tree ok until a walker says otherwise
+  }
+  __syncthreads();
+  if (tid < a.N) {
+    uint32_t m[4];
+    bool good = ancestor_mask(a, b, tid, m);
+    anc[4 * tid + 0] = m[0]; anc[4 * tid + 1] = m[1];
+    anc[4 * tid + 2] = m[2]; anc[4 * tid + 3] = m[3];
+    if (!good) misc[3] = 0;
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + OFF_MISC, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();   // the peer's barriers are initialised before any remote arrive
+
+  const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+  const bool ok = misc[1] && misc[3];
+  const int L = misc[2];
+  const int T = L + a.N;
+  const int k0 = s * a.chunk;
+  const int k1 = min(T, k0 + a.chunk);
+  const int nt = (ok && k1 > k0) ? (k1 - k0 + BN - 1) / BN : 0;
+  const long long req_row0 = (long long)b * a.N * a.H;    // first global row of request b
+
+  if (warp == 0) {
+    // ---- TMA producer --------------------------------------------------------------
+    if (lane == 0 && nt > 0) {
+      prefetch_tmap(&tm_qlat);
+      prefetch_tmap(&tm_ckv);
+      const int qrow = (int)(req_row0 + (long long)rt * BM);
+      mbar_expect_tx(BAR(B_Q_FULL), nch * kQChunk);
+      for (int c = 0; c < 4; ++c)
+        tma_load_2d(sbase + OFF_Q + c * kQChunk, &tm_qlat, BAR(B_Q_FULL),
+                    (int)rank * kHalf + c * CH, qrow);
+      if (rank == 0)
+        tma_load_2d(sbase + OFF_Q + 4 * kQChunk, &tm_qrope, BAR(B_Q_FULL), 0, qrow);
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int stg = j & 1;
+        if (j >= kStages &&
+            !wait(BAR(B_KV_EMPTY + stg), ((j >> 1) - 1) & 1, st, limit, W_KV_EMPTY))
+          break;
+        const int t0 = k0 + j * BN;
+        int row;
+        if (a.page_size) {
+          row = a.page_table[(long long)b * a.max_pages + t0 / a.page_size] * a.page_size;
+        } else {
+          row = b * a.t_stride + t0;
+        }
+        mbar_expect_tx(BAR(B_KV_FULL + stg), nch * kKVChunk);
+        const uint32_t dst = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
+                      (int)rank * kHalf + c * CH, row);
+        if (rank == 0) tma_load_2d(dst + 4 * kKVChunk, &tm_krope, BAR(B_KV_FULL + stg), 0, row);
+        issued = j + 1;
+      }
+      // Drain: every issued copy has landed before this CTA may exit.
+      wait(BAR(B_Q_FULL), 0, st, limit, W_DRAIN);
+      for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+        wait(BAR(B_KV_FULL + (j & 1)), (j >> 1) & 1, st, limit, W_DRAIN);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---- MMA issuer ----------------------------------------------------------------
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
+      bool alive = wait(BAR(B_Q_FULL), 0, st, limit, W_Q);
+      for (int j = 0; alive && j <= nt; ++j) {
+        if (j < nt) {
+          const int stg = j & 1;
+          alive = wait(BAR(B_KV_FULL + stg), (j >> 1) & 1, st, limit, W_KV_FULL);
+          if (alive && j >= kStages)
+            alive = wait(BAR(B_S_EMPTY + stg), ((j >> 1) - 1) & 1, st, limit, W_S_EMPTY);
+          if (!alive) break;
+          tc_fence_after();
+          const uint32_t d = tmem + kColS + stg * BN;
+          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+          for (int c = 0; c < nch; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < CH / 16; ++kk) {
+              uint64_t ad = smem_desc(sbase + OFF_Q + c * kQChunk + kk * 32, 16, 1024);
+              uint64_t bd = smem_desc(kv + c * kKVChunk + kk * 32, 16, 1024);
+              mma_bf16(d, ad, bd, kIdescQK, (c | kk) != 0);
+            }
+          }
+          mma_commit(BAR(B_S_FULL + stg));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, stg = jj & 1;
+          alive = wait(BAR(B_P_FULL), jj & 1, st, limit, W_P_FULL);
+          if (!alive) break;
+          tc_fence_after();
+          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            uint64_t ad = smem_desc(sbase + OFF_P + kk * 32, 16, 1024);
+            // V = c_kv columns of this CTA, MN-major: 64-column chunks are
+            // kKVChunk apart (LBO), 8-key groups 1024 B apart (SBO).
+            uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
+            mma_bf16(tmem + kColO, ad, bd, kIdescPV, (jj > 0 || kk > 0));
+          }
+          mma_commit(BAR(B_KV_EMPTY + stg));
+          mma_commit(BAR(B_P_EMPTY));
+        }
+      }
+      if (alive) mma_commit(BAR(B_O_FULL));
+      mma_commit(BAR(B_MMA_DONE));               // drain every issued MMA
+      wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
+    }
+    __syncwarp();
+  } else {
+    // ---- softmax / exchange / epilogue (warps 2..5) ----------------------------------
+    const int q = warp & 3;                      // TMEM lane quadrant of this warp
+    const int r = q * 32 + lane;                 // row within the tile = TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    const int rr = rt * BM + r;                  // row within the request
+    const bool row_valid = rr < a.N * a.H;
+    const int node = row_valid ? rr / a.H : 0;
+    uint32_t my_anc[4] = {0u, 0u, 0u, 0u};
+    if (ok && row_valid) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) my_anc[w] = anc[4 * node + w];
+    }
+    const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
+    float m_used = -INFINITY, l_sum = 0.f;
+    bool alive = true;
+    const uint32_t rx_local = sbase + OFF_RX + r * kRxStride * 4;
+    const uint32_t rx_remote = mapa(rx_local, peer);
+    const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL), peer);
+    const uint32_t txok_remote = mapa(BAR(B_TX_OK), peer);
+    const uint32_t p_row = sbase + OFF_P + r * 128;
+
+    if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL)) {
+      alive = wait(BAR(B_STALL), 0, st, limit, W_STALL);   // nothing arrives here
+      alive = __all_sync(0xffffffffu, alive);
+    }
+
+    for (int j = 0; alive && j < nt; ++j) {
+      const int stg = j & 1;
+      alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + stg), (j >> 1) & 1, st, limit, W_S_FULL));
+      if (!alive) break;
+      tc_fence_after();
+      float sv[64];
+      {
+        float t0v[32], t1v[32];
+        tmem_ld32(tmem + lane_addr + kColS + stg * BN, t0v);
+        tmem_ld32(tmem + lane_addr + kColS + stg * BN + 32, t1v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) { sv[k] = t0v[k]; sv[32 + k] = t1v[k]; }
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(B_S_EMPTY + stg));
+
+      // exchange the partial scores with the peer CTA
+      if (j >= 1) {
+        alive = __all_sync(0xffffffffu, wait<true>(BAR(B_TX_OK), (j - 1) & 1, st, limit, W_TX_OK));
+        if (!alive) break;
+      }
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(rx_remote + 16 * v), "f"(sv[4 * v]), "f"(sv[4 * v + 1]),
+                        "f"(sv[4 * v + 2]), "f"(sv[4 * v + 3]) : "memory");
+      }
+      mbar_arrive_remote(rxfull_remote);
+      alive = __all_sync(0xffffffffu, wait<true>(BAR(B_RX_FULL), j & 1, st, limit, W_RX_FULL));
+      if (!alive) break;
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        float x0, x1, x2, x3;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3) : "r"(rx_local + 16 * v)
+                     : "memory");
+        sv[4 * v] += x0; sv[4 * v + 1] += x1; sv[4 * v + 2] += x2; sv[4 * v + 3] += x3;
+      }
+      mbar_arrive_remote(txok_remote);
+
+      // visibility mask, scale, tile max
+      const int t0 = k0 + j * BN;
+      float m_tile = -INFINITY;
+      if (row_valid && t0 + BN <= L) {
+#pragma unroll
+        for (int k = 0; k < BN; ++k) { sv[k] *= sl2; m_tile = fmaxf(m_tile, sv[k]); }
+      } else {
+#pragma unroll
+        for (int k = 0; k < BN; ++k) {
+          const int t = t0 + k;
+          bool vis = false;
+          if (row_valid && t < k1) {
+            if (t < L) vis = true;
+            else { const int jn = t - L; vis = (my_anc[jn >> 5] >> (jn & 31)) & 1u; }
+          }
+          sv[k] = vis ? sv[k] * sl2 : -INFINITY;
+          m_tile = fmaxf(m_tile, sv[k]);
+        }
+      }
+      // lazy rescale: move the reference max only when it grows by > 8 (log2)
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_tile > m_used + 8.f) {
+        if (m_used != -INFINITY) { alpha = exp2f(m_used - m_tile); rescale = true; }
+        l_sum *= alpha;
+        m_used = m_tile;
+      }
+      uint32_t packed[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int k = 0; k < BN; k += 2) {
+        float p0 = (sv[k] == -INFINITY) ? 0.f : exp2f(sv[k] - m_used);
+        float p1 = (sv[k + 1] == -INFINITY) ? 0.f : exp2f(sv[k + 1] - m_used);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+        psum += __low2float(h2) + __high2float(h2);
+        packed[k >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      l_sum += psum;
+
+      // P and O are free once the previous P.V has completed
+      if (j >= 1) {
+        alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY), (j - 1) & 1, st, limit, W_P_EMPTY));
+        if (!alive) break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, rescale)) {
+        for (int c = 0; c < kHalf / 32; ++c) {
+          float ov[32];
+          tmem_ld32(tmem + lane_addr + kColO + 32 * c, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+          tmem_st32(tmem + lane_addr + kColO + 32 * c, ov);
+        }
+        tmem_wait_st();
+      }
+      // P row: 64 bf16 = eight 16-byte chunks, 128-byte swizzle (chunk ^ row%8)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t addr = p_row + ((c ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(addr), "r"(packed[4 * c]), "r"(packed[4 * c + 1]),
+                        "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3]) : "memory");
+      }
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(BAR(B_P_FULL));
+    }
+
+    // ---- epilogue: unnormalised partial o_lat half, (m, l) -----------------------------
+    if (alive && nt > 0)
+      alive = __all_sync(0xffffffffu, wait(BAR(B_O_FULL), 0, st, limit, W_O_FULL));
+    // tcgen05.ld is warp-collective: every lane loads, only valid rows store.
+    const bool has_data = ok && alive && nt > 0 && row_valid && l_sum > 0.f;
+    if (ok && alive && row_valid) {
+      const long long rows = (long long)a.B * a.N * a.H;
+      float* ml = a.part_ml + ((long long)s * rows + req_row0 + rr) * 2;
+      if (rank == 0) {
+        ml[0] = has_data ? m_used * 0.6931471805599453f : -INFINITY;
+        ml[1] = has_data ? l_sum : 0.f;
+      }
+    }
+    if (ok && alive && nt > 0 && __any_sync(0xffffffffu, has_data)) {
+      const long long rows = (long long)a.B * a.N * a.H;
+      float* po = a.part_o + ((long long)s * rows + req_row0 + (has_data ? rr : 0)) * a.d_c +
+                  rank * kHalf;
+      tc_fence_after();
+      for (int c = 0; c < kHalf / 32; ++c) {
+        float ov[32];
+        tmem_ld32(tmem + lane_addr + kColO + 32 * c, ov);
+        tmem_wait_ld();
+        if (has_data) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(po + 32 * c + k) =
+                make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
+        }
+      }
+    }
+  }
+
+  // ---- teardown ------------------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  cluster_sync();   // the peer may still arrive on our barriers until here
+}
+
+// The driver's tensor-map encoder, resolved through the runtime so that the
+// library does not link libcuda (it must load on hosts without a driver).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+CUresult encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int row_tiles_of(const kdtv_dims* d) { return (d->N * d->H + BM - 1) / BM; }
+
+}  // namespace
+
+int tc_supported(const kdtv_dims* d) {
+  if (d->dtype != KDTV_BF16 || d->d_c != 512 || d->d_rope != 64) return 0;
+  if (d->page_size != 0 && d->page_size != 64) return 0;
+  if (d->kv_chunk % BN) return 0;
+  return 1;
+}
+
+int tc_launches(const kdtv_dims*) { return 4; }
+
+// Split-KV chunk: pick the split count s that minimises the modelled
+// makespan  ceil(2 * items(s) / SMs) / s  (two CTAs per item, one CTA per
+// SM), with a small per-split cost for the partials it writes and merges.
+int tc_chunk(const kdtv_dims* d, int sms) {
+  const long long base = (long long)d->B * row_tiles_of(d);
+  const int t_cap = d->page_size ? d->max_pages * d->page_size : d->t_stride;
+  const int max_s = (t_cap + 511) / 512;
+  int best_s = 1;
+  double best = 1e30;
+  for (int s = 1; s <= (max_s < 64 ? max_s : 64); ++s) {
+    const double waves = (double)((2 * base * s + sms - 1) / sms);
+    const double cost = waves / s + 0.02 * s;
+    if (cost < best - 1e-9) { best = cost; best_s = s; }
+  }
+  int chunk = (t_cap + best_s - 1) / best_s;
+  return (chunk + BN - 1) / BN * BN;
+}
+
+cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t* ev) {
+  for (const void* ptr : {a.q_rope, a.c_kv, a.k_rope, static_cast<const void*>(a.q_lat)})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return cudaErrorMisalignedAddress;
+  const long long rows = (long long)a.B * a.N * a.H;
+  const long long kv_rows = a.page_size ? (long long)a.num_pages * a.page_size
+                                        : (long long)a.B * a.t_stride;
+  CUtensorMap tq, tqr, tck, tkr;
+  if (encode_2d(&tq, a.q_lat, rows, 512, CH, BM) != CUDA_SUCCESS ||
+      encode_2d(&tqr, a.q_rope, rows, 64, CH, BM) != CUDA_SUCCESS ||
+      encode_2d(&tck, a.c_kv, kv_rows, 512, CH, BN) != CUDA_SUCCESS ||
+      encode_2d(&tkr, a.k_rope, kv_rows, 64, CH, BN) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  cudaError_t e = launch_absorb(a, st, /*bf16_out=*/true);
+  if (e != cudaSuccess) return e;
+  if (ev) cudaEventRecord(ev[1], st);
+
+  TcCfg cfg;
+  cfg.row_tiles = (a.N * a.H + BM - 1) / BM;
+  cfg.limit_ns = (a.flags & KDTV_FLAG_TEST_STALL) ? 20000000ull : 2000000000ull;
+  const long long items = (long long)a.B * cfg.row_tiles * a.splits;
+  if (2 * items > 0x7fffffffll) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e != cudaSuccess) return e;
+  attn_tc_kernel<<<(unsigned)(2 * items), kThreads, kSmemBytes, st>>>(tq, tqr, tck, tkr, a, cfg);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (ev) cudaEventRecord(ev[2], st);
+  return launch_combine_uproj(a, p, st, ev);
+}
+
+}  // namespace kdtv

@@ -1,0 +1,121 @@
+"""C-ABI boundary checks that need no GPU: the library builds, loads, exports
+every symbol include/kdtv.h declares, and rejects bad arguments on the host
+before any CUDA work."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_tree_mla_gb300 import kdtv, workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from speculative_decoding_tree_mla_gb300 import build
+    build.build()
+    return kdtv.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kdtv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kdtv_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert names, "no functions parsed from kdtv.h"
+    assert set(names) == set(kdtv.EXPORTS)
+    for n in names:
+        assert hasattr(L, n), f"{n} not exported"
+
+
+def _dims(name="kimi_single", **kw):
+    wl_spec = W.SPECS[name]
+    kw.setdefault("flags", kdtv.KDTV_FLAG_SIMT)
+    d = kdtv.make_dims(wl_spec, dtype=wl_spec.dtype, t_stride=kw.pop("t_stride", 8192),
+                       **kw)
+    return d
+
+
+@pytest.mark.parametrize("flags", [0, kdtv.KDTV_FLAG_SIMT])
+def test_workspace_sizes(L, flags):
+    if flags == 0 and kdtv.workspace_size(_dims(flags=0)) == 0:
+        pytest.skip("tensor-core path not compiled in")
+    for name, spec in W.SPECS.items():
+        if spec.paged:
+            d = kdtv.make_dims(spec, dtype=spec.dtype, page_size=64, max_pages=520,
+                               num_pages=10000, flags=flags)
+        else:
+            d = kdtv.make_dims(spec, dtype=spec.dtype, t_stride=65664, flags=flags)
+        n = kdtv.workspace_size(d)
+        assert n > 0 and n % 256 == 0
+        assert kdtv.launches_per_call(d) > 0
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("N", 0, "KDTV_ERR_INVALID_ARG"),
+    ("H", -1, "KDTV_ERR_INVALID_ARG"),
+    ("N", 129, "KDTV_ERR_UNSUPPORTED"),
+    ("dtype", 7, "KDTV_ERR_INVALID_ARG"),
+    ("t_stride", 3, "KDTV_ERR_INVALID_ARG"),
+    ("d_c", 1024, "KDTV_ERR_UNSUPPORTED"),
+])
+def test_bad_dims_rejected_on_host(L, field, value, code):
+    d = _dims()
+    setattr(d, field, value)
+    assert kdtv.workspace_size(d) == 0
+    fake = 256
+    rc = kdtv.verify_attn_raw(d, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, 0)
+    assert kdtv.STATUS[rc] == code
+
+
+def test_null_pointers_and_workspace_rejected(L):
+    d = _dims()
+    fake = 256
+    # no workspace set
+    rc = kdtv.verify_attn_raw(d, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, 0)
+    assert kdtv.STATUS[rc] == "KDTV_ERR_INVALID_ARG"
+    d.workspace = 4096
+    d.workspace_bytes = kdtv.workspace_size(d)
+    rc = kdtv.verify_attn_raw(d, 0, fake, fake, fake, fake, fake, fake, fake, 0, fake, 0)
+    assert kdtv.STATUS[rc] == "KDTV_ERR_INVALID_ARG"
+    # page_table given for a contiguous cache
+    rc = kdtv.verify_attn_raw(d, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 0)
+    assert kdtv.STATUS[rc] == "KDTV_ERR_INVALID_ARG"
+    # workspace too small / misaligned
+    d.workspace_bytes = 1024
+    rc = kdtv.verify_attn_raw(d, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, 0)
+    assert kdtv.STATUS[rc] == "KDTV_ERR_INVALID_ARG"
+    d.workspace = 4096 + 16
+    d.workspace_bytes = 1 << 40
+    rc = kdtv.verify_attn_raw(d, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, 0)
+    assert kdtv.STATUS[rc] == "KDTV_ERR_INVALID_ARG"
+
+
+def test_strerror(L):
+    for code, name in kdtv.STATUS.items():
+        assert kdtv.strerror(code) == name
+
+
+def test_workloads_deterministic():
+    a = W.make("tiny")
+    b = W.make("tiny")
+    for k in a.t:
+        assert (a.t[k] == b.t[k]).all()
+    c = W.make("tiny", seed=123)
+    assert not (a.t["c_kv"] == c.t["c_kv"]).all()
+
+
+def test_product_path_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "speculative_decoding_tree_mla_gb300")
+    for dp, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                txt = open(os.path.join(dp, f)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, re.M), f
+                assert "mla_tree_attn" not in txt, f
