@@ -68,6 +68,9 @@ enum kdtv_status {
 /* kdtv_dims.flags */
 #define KDTV_FLAG_SIMT 0x1u          /* bf16 inputs on the CUDA-core path (the
                                         tensor-core path is the default)          */
+#define KDTV_FLAG_SIMT_PROJ 0x2u     /* bf16: tensor-core attention, but the absorb,
+                                        split combine and up-projection on CUDA
+                                        cores                                     */
 #define KDTV_FLAG_TEST_STALL 0x100u  /* TEST ONLY: the attention kernel waits on a
                                         barrier that nothing arrives on, with a
                                         ~20 ms limit, so the timeout path can be
@@ -145,6 +148,66 @@ const char* kdtv_strerror(int status);
 /* Number of kernels kdtv_verify_attn launches for these dims (for launch
  * accounting), or -1 if the dims are invalid. */
 int kdtv_launches_per_call(const kdtv_dims* dims);
+
+/* ---- the loop steps around the verify attention -------------------------------------
+ * "The Moment of Proof: Validating a Native CUDA Speculative Decoding Engine",
+ * section "The Context: Building a Native DDTree Engine from Scratch", names a
+ * GPU best-first tree builder, a greedy tree-accept kernel and post-verify KV
+ * cache compaction.  Each runs one CTA per request (trees have <= 128 nodes).
+ */
+
+/*
+ * kdtv_tree_accept — greedy acceptance ("The Build That Proved It: Compiling
+ * the Native DDTree Speculative Decoding Engine", section "The Output Knowledge
+ * Created": the accept kernel keeps the longest prefix match).  Node 0 is the
+ * root (the last committed token).  From node u the walk moves to the
+ * lowest-indexed child c of u with draft_tok[c] == target_argmax[u] and stops
+ * when there is none.
+ *   parent, draft_tok, target_argmax  [B, N] int32 (device)
+ *   path      [B, N] int32 out: accepted node indices (path[0] = 0), then -1
+ *   path_len  [B] int32 out: accepted nodes including the root
+ *   bonus     [B] int32 out: target_argmax at the last accepted node
+ * Commits path_len - 1 draft tokens plus the bonus token.  parent[] is only
+ * compared, never dereferenced, so a malformed tree cannot fault.  Returns
+ * KDTV_ERR_INVALID_ARG / KDTV_ERR_UNSUPPORTED (N > 128) / KDTV_ERR_CUDA.
+ */
+int kdtv_tree_accept(int B, int N, const int32_t* parent, const int32_t* draft_tok,
+                     const int32_t* target_argmax, int32_t* path, int32_t* path_len,
+                     int32_t* bonus, cudaStream_t stream);
+
+/*
+ * kdtv_compact_kv — post-verify KV compaction, in place ("The Moment of
+ * Truth: Validating a Custom CUDA Inference Engine for Kimi K2.6", section
+ * "What the Output Tells Us": kept rows are gathered into a compact cache
+ * without an in-place race).  For each request b the latent rows at positions
+ * prefix_len[b] + path[b][k] move to prefix_len[b] + k, k < path_len[b]; all
+ * other rows are untouched.  Uses dims->B, N, d_c, d_rope, dtype, page_size,
+ * t_stride, max_pages, num_pages (same layouts as kdtv_verify_attn); c_kv and
+ * k_rope are modified in place.  path must be strictly increasing with
+ * path[k] >= k (as kdtv_tree_accept produces).  Device-side problems (bad
+ * path, prefix overflow, bad page id) leave that request untouched and set
+ * *status (device word, first error wins) to KDTV_ERR_BAD_TREE /
+ * KDTV_ERR_BAD_PREFIX / KDTV_ERR_BAD_PAGE.  Requests must not share pages.
+ */
+int kdtv_compact_kv(const kdtv_dims* dims, void* c_kv, void* k_rope,
+                    const int32_t* prefix_len, const int32_t* path, const int32_t* path_len,
+                    const int32_t* page_table, unsigned int* status, cudaStream_t stream);
+
+/*
+ * kdtv_tree_build — best-first draft tree from per-depth top-K proposals.
+ * Node 0 is the root (root_token[b], depth 0, score 0).  A node at depth d < D
+ * offers K candidate children (tokens[b][d][k], score + logp[b][d][k], float32
+ * addition); the best candidate (highest score, then lower parent index, then
+ * lower k) becomes the next node until N nodes exist or no candidate is left.
+ *   logp [B, D, K] float32, tokens [B, D, K] int32, root_token [B] int32
+ *   parent, token, depth [B, N] int32 out; score [B, N] float32 out (node
+ *   order is topological; unused slots are -1 / -inf); n_nodes [B] int32 out.
+ * Returns KDTV_ERR_INVALID_ARG, KDTV_ERR_UNSUPPORTED (N > 128, K > 64) or
+ * KDTV_ERR_CUDA.
+ */
+int kdtv_tree_build(int B, int D, int K, int N, const float* logp, const int32_t* tokens,
+                    const int32_t* root_token, int32_t* parent, int32_t* token,
+                    int32_t* depth, float* score, int32_t* n_nodes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

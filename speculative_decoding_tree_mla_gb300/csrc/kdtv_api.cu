@@ -100,7 +100,7 @@ extern "C" size_t kdtv_workspace_size(const kdtv_dims* d) {
 extern "C" int kdtv_launches_per_call(const kdtv_dims* d) {
   Plan p;
   if (make_plan(d, &p) != KDTV_OK) return -1;
-  return p.tensor_core ? tc_launches(d) : 4;
+  return p.tensor_core ? tc_launches(d, p.splits) : 4;
 }
 
 extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const void* q_rope,

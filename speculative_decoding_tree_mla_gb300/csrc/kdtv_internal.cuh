@@ -125,8 +125,13 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t s,
 cudaError_t launch_absorb(const Args& a, cudaStream_t s, bool bf16_out);
 cudaError_t launch_combine_uproj(const Args& a, const Plan& p, cudaStream_t s,
                                  cudaEvent_t* ev);
+cudaError_t launch_absorb_tc(const Args& a, cudaStream_t s);
+cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t s,
+                                    cudaEvent_t* ev);
+bool absorb_tc_ok(const Args& a);
+bool combine_uproj_tc_ok(const Args& a);
 int tc_supported(const kdtv_dims* d);
-int tc_launches(const kdtv_dims* d);
+int tc_launches(const kdtv_dims* d, int splits);
 int tc_chunk(const kdtv_dims* d, int sm_count);
 
 }  // namespace kdtv

@@ -33,6 +33,7 @@
 
 #include "kdtv_internal.cuh"
 #include "kdtv_ptx.cuh"
+#include "kdtv_tmap.cuh"
 
 namespace kdtv {
 namespace {
@@ -429,6 +430,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
   cluster_sync();   // the peer may still arrive on our barriers until here
 }
 
+int row_tiles_of(const kdtv_dims* d) { return (d->N * d->H + BM - 1) / BM; }
+
+}  // namespace
+
+namespace {
 // The driver's tensor-map encoder, resolved through the runtime so that the
 // library does not link libcuda (it must load on hosts without a driver).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -449,22 +455,22 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
+}  // namespace
+
+// 2-D bf16 tensor map with a 128-byte swizzle: rows x cols (row stride
+// cols * 2 bytes), box = box_rows x box_cols.
 CUresult encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                   uint32_t box_cols, uint32_t box_rows) {
+                   uint32_t box_cols, uint32_t box_rows, uint64_t row_stride_elems) {
   EncodeTiledFn fn = encoder();
   if (!fn) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {(row_stride_elems ? row_stride_elems : cols) * 2};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
-
-int row_tiles_of(const kdtv_dims* d) { return (d->N * d->H + BM - 1) / BM; }
-
-}  // namespace
 
 int tc_supported(const kdtv_dims* d) {
   if (d->dtype != KDTV_BF16 || d->d_c != 512 || d->d_rope != 64) return 0;
@@ -473,7 +479,12 @@ int tc_supported(const kdtv_dims* d) {
   return 1;
 }
 
-int tc_launches(const kdtv_dims*) { return 4; }
+int tc_launches(const kdtv_dims* d, int splits) {
+  if (d->flags & KDTV_FLAG_SIMT_PROJ) return 4;
+  Args a;
+  a.dtype = d->dtype; a.d_c = d->d_c; a.d_v = d->d_v; a.d_nope = d->d_nope; a.splits = splits;
+  return 2 + (combine_uproj_tc_ok(a) ? 1 : 2);
+}
 
 // Split-KV chunk: pick the split count s that minimises the modelled
 // makespan  ceil(2 * items(s) / SMs) / s  (two CTAs per item, one CTA per
@@ -506,7 +517,8 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
       encode_2d(&tkr, a.k_rope, kv_rows, 64, CH, BN) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
-  cudaError_t e = launch_absorb(a, st, /*bf16_out=*/true);
+  const bool simt_proj = a.flags & KDTV_FLAG_SIMT_PROJ;
+  cudaError_t e = simt_proj ? launch_absorb(a, st, /*bf16_out=*/true) : launch_absorb_tc(a, st);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[1], st);
 
@@ -522,7 +534,7 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], st);
-  return launch_combine_uproj(a, p, st, ev);
+  return simt_proj ? launch_combine_uproj(a, p, st, ev) : launch_combine_uproj_tc(a, p, st, ev);
 }
 
 }  // namespace kdtv

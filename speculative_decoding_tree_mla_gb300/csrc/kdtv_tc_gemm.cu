@@ -1,0 +1,288 @@
+// Tensor-core (tcgen05) kernels for the two per-head projections around the
+// attention, the absorbed form's w_kc / w_vc halves ("The Moment of Proof:
+// Validating a Native CUDA Speculative Decoding Engine", section "Input
+// Knowledge Required"):
+//
+//   absorb_tc_kernel          q_lat[r, h, :] = W_UK[h]^T q_nope[r, h, :]   (bf16 out)
+//   combine_uproj_tc_kernel   o_lat = log-sum-exp merge of the split partials,
+//                             out[r, h, :] = W_UV[h] o_lat                  (fp32 out)
+//
+// Both run transposed so the weight matrix is the 128-row MMA operand and the
+// query rows are the MMA N dimension: D[128 x rows] = W-block . X^T, with the
+// weight tile loaded by TMA (W_UK read as an MN-major operand) and the result
+// read back lane-per-output-feature, which makes the global writes coalesced.
+
+#include <cuda.h>
+
+#include "kdtv_internal.cuh"
+#include "kdtv_ptx.cuh"
+#include "kdtv_tmap.cuh"
+
+namespace kdtv {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 128;
+constexpr uint64_t kLimitNs = 2000000000ull;
+
+// ---- A1: absorb -----------------------------------------------------------------------
+constexpr int AB_M = 128;                  // latent columns per CTA
+constexpr int AB_NR = 128;                 // query rows (b, i) per CTA
+constexpr int AB_OFF_B = 2 * 256 * 128;    // A: two MN atoms of up to 256 e-rows x 128 B
+constexpr int AB_OFF_BAR = AB_OFF_B + 4 * AB_NR * 128;
+constexpr int AB_SMEM = AB_OFF_BAR + 64 + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1)
+absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
+                 const Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d0 = blockIdx.x * AB_M;
+  const int h = blockIdx.y;
+  const int r0 = blockIdx.z * AB_NR;
+  const int BNr = a.B * a.N;
+  const int nr = min(AB_NR, BNr - r0);
+  const int n_mma = (nr + 15) & ~15;
+  const int kch = a.d_nope / 64;             // 64-wide K chunks
+  const uint32_t bar_full = sbase + AB_OFF_BAR, bar_mma = bar_full + 8;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + AB_OFF_BAR + 16);
+
+  if (tid == 0) {
+    mbar_init(bar_full, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) { tmem_alloc(sbase + AB_OFF_BAR + 16, AB_NR); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  bool ok = true;
+  if (tid == 0) {
+    const uint32_t a_bytes = 2u * a.d_nope * 128u;
+    mbar_expect_tx(bar_full, a_bytes + kch * AB_NR * 128u);
+    for (int c = 0; c < 2; ++c)       // W_UK[h][:, d0 + 64c : +64]: e-rows x 64 d
+      tma_load_2d(sbase + c * a.d_nope * 128, &tm_w, bar_full, d0 + 64 * c, h * a.d_nope);
+    for (int k = 0; k < kch; ++k)     // q_nope rows r0.. of head h, e in [64k, 64k+64)
+      tma_load_2d(sbase + AB_OFF_B + k * AB_NR * 128, &tm_q, bar_full, h * a.d_nope + 64 * k, r0);
+    ok = wait(bar_full, 0, a.status, kLimitNs, 101);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(AB_M, n_mma, /*a_mn=*/1, /*b_mn=*/0);
+      for (int kk = 0; kk < a.d_nope / 16; ++kk) {
+        // A (MN-major): 64-column atoms a.d_nope*128 B apart, 8 e-rows per 1 KiB.
+        uint64_t ad = smem_desc(sbase + kk * 16 * 128, a.d_nope * 128, 1024);
+        uint64_t bd = smem_desc(sbase + AB_OFF_B + (kk >> 2) * AB_NR * 128 + (kk & 3) * 32, 16, 1024);
+        mma_bf16(tmem, ad, bd, idesc, kk > 0);
+      }
+    }
+    mma_commit(bar_mma);
+  }
+  __syncwarp();
+  ok = wait(bar_mma, 0, a.status, kLimitNs, 102) && ok;
+  ok = __all_sync(0xffffffffu, ok);
+  tc_fence_after();
+  if (ok) {
+    __nv_bfloat16* ql = static_cast<__nv_bfloat16*>(a.q_lat);
+    const int d = d0 + warp * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    for (int c0 = 0; c0 < n_mma; c0 += 32) {
+      float v[32];
+      tmem_ld32(tmem + lane_addr + c0, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int r = c0 + j;
+        if (r < nr) ql[((long long)(r0 + r) * a.H + h) * 512 + d] = __float2bfloat16_rn(v[j]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tmem, AB_NR); }
+}
+
+// ---- A5 + A6: split combine fused with the W_UV up-projection -------------------------
+constexpr int UP_NR = 64;                          // query rows (b, i) per CTA
+constexpr int UP_MAX_SPLITS = 64;
+constexpr int UP_OFF_B = 8 * 128 * 128;            // A: W_UV[h] as 8 chunks of 128 v x 64 d
+constexpr int UP_OFF_W = UP_OFF_B + 8 * UP_NR * 128;
+constexpr int UP_OFF_BAR = UP_OFF_W + UP_NR * UP_MAX_SPLITS * 4;
+constexpr int UP_SMEM = UP_OFF_BAR + 64 + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1)
+combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.x;
+  const int r0 = blockIdx.y * UP_NR;
+  const int BNr = a.B * a.N;
+  const int nr = min(UP_NR, BNr - r0);
+  const int S = a.splits;
+  const long long rows = (long long)BNr * a.H;
+  float* wts = reinterpret_cast<float*>(sm + UP_OFF_W);
+  const uint32_t bar_full = sbase + UP_OFF_BAR, bar_mma = bar_full + 8;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + UP_OFF_BAR + 16);
+
+  if (tid == 0) {
+    mbar_init(bar_full, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) { tmem_alloc(sbase + UP_OFF_BAR + 16, UP_NR); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (tid == 0) {   // W_UV[h]: 128 v-rows x 512 d, eight 64-column chunks
+    mbar_expect_tx(bar_full, 8 * 128 * 128);
+    for (int k = 0; k < 8; ++k)
+      tma_load_2d(sbase + k * 128 * 128, &tm_w, bar_full, 64 * k, h * 128);
+  }
+
+  // Split weights per row, with 1 / sum_s e^{m_s - m*} l_s folded in.
+  if (tid < UP_NR) {
+    const int r = tid;
+    float* w = wts + r * UP_MAX_SPLITS;
+    if (r < nr) {
+      const long long grow = (long long)(r0 + r) * a.H + h;
+      float m = -INFINITY;
+      for (int s = 0; s < S; ++s) {
+        const float* ml = a.part_ml + ((long long)s * rows + grow) * 2;
+        if (ml[1] > 0.f) m = fmaxf(m, ml[0]);
+      }
+      float l = 0.f;
+      for (int s = 0; s < S; ++s) {
+        const float* ml = a.part_ml + ((long long)s * rows + grow) * 2;
+        const float e = ml[1] > 0.f ? expf(ml[0] - m) : 0.f;
+        w[s] = e;
+        l += e * ml[1];
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      for (int s = 0; s < S; ++s) w[s] *= inv;
+    } else {
+      for (int s = 0; s < S; ++s) w[s] = 0.f;
+    }
+  }
+  __syncthreads();
+
+  // o_lat rows -> bf16, 128-byte swizzled K-major operand: row r, 8-column unit u.
+  for (int idx = tid; idx < UP_NR * 64; idx += kThreads) {
+    const int r = idx >> 6, u = idx & 63;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (r < nr) {
+      const long long grow = (long long)(r0 + r) * a.H + h;
+      const float* w = wts + r * UP_MAX_SPLITS;
+      for (int s = 0; s < S; ++s) {
+        const float ws = w[s];
+        if (ws == 0.f) continue;
+        const float4* src =
+            reinterpret_cast<const float4*>(a.part_o + ((long long)s * rows + grow) * 512 + 8 * u);
+        const float4 x0 = src[0], x1 = src[1];
+        acc[0] = fmaf(ws, x0.x, acc[0]); acc[1] = fmaf(ws, x0.y, acc[1]);
+        acc[2] = fmaf(ws, x0.z, acc[2]); acc[3] = fmaf(ws, x0.w, acc[3]);
+        acc[4] = fmaf(ws, x1.x, acc[4]); acc[5] = fmaf(ws, x1.y, acc[5]);
+        acc[6] = fmaf(ws, x1.z, acc[6]); acc[7] = fmaf(ws, x1.w, acc[7]);
+      }
+    }
+    uint32_t pk[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+      pk[j] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    const uint32_t addr = sbase + UP_OFF_B + (u >> 3) * UP_NR * 128 + r * 128 +
+                          (((u & 7) ^ (r & 7)) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                 :: "r"(addr), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]) : "memory");
+  }
+  fence_async_smem();
+  __syncthreads();
+
+  bool ok = true;
+  if (tid == 0) {
+    ok = wait(bar_full, 0, a.status, kLimitNs, 111);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(128, UP_NR, 0, 0);
+      for (int kk = 0; kk < 32; ++kk) {
+        uint64_t ad = smem_desc(sbase + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
+        uint64_t bd = smem_desc(sbase + UP_OFF_B + (kk >> 2) * UP_NR * 128 + (kk & 3) * 32, 16, 1024);
+        mma_bf16(tmem, ad, bd, idesc, kk > 0);
+      }
+    }
+    mma_commit(bar_mma);
+  }
+  __syncwarp();
+  ok = wait(bar_mma, 0, a.status, kLimitNs, 112) && ok;
+  ok = __all_sync(0xffffffffu, ok);
+  tc_fence_after();
+  if (ok) {
+    const int v = warp * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    for (int c0 = 0; c0 < UP_NR; c0 += 32) {
+      float x[32];
+      tmem_ld32(tmem + lane_addr + c0, x);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int r = c0 + j;
+        if (r < nr) a.out[((long long)(r0 + r) * a.H + h) * 128 + v] = x[j];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tmem, UP_NR); }
+}
+
+}  // namespace
+
+bool absorb_tc_ok(const Args& a) {
+  return a.dtype == KDTV_BF16 && a.d_c == 512 && a.d_nope % 64 == 0 && a.d_nope <= 256;
+}
+
+bool combine_uproj_tc_ok(const Args& a) {
+  return a.dtype == KDTV_BF16 && a.d_c == 512 && a.d_v == 128 && a.splits <= UP_MAX_SPLITS;
+}
+
+cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st) {
+  if (!absorb_tc_ok(a)) return launch_absorb(a, st, /*bf16_out=*/true);
+  CUtensorMap tw, tq;
+  const uint64_t BNr = (uint64_t)a.B * a.N;
+  if (encode_2d(&tw, a.W_UK, (uint64_t)a.H * a.d_nope, 512, 64, a.d_nope) != CUDA_SUCCESS ||
+      encode_2d(&tq, a.q_nope, BNr, (uint64_t)a.H * a.d_nope, 64, AB_NR) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(absorb_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, AB_SMEM);
+  if (e != cudaSuccess) return e;
+  dim3 grid(512 / AB_M, a.H, (unsigned)((BNr + AB_NR - 1) / AB_NR));
+  absorb_tc_kernel<<<grid, kThreads, AB_SMEM, st>>>(tw, tq, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t st,
+                                    cudaEvent_t* ev) {
+  if (!combine_uproj_tc_ok(a)) return launch_combine_uproj(a, p, st, ev);
+  CUtensorMap tw;
+  if (encode_2d(&tw, a.W_UV, (uint64_t)a.H * 128, 512, 64, 128) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(combine_uproj_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, UP_SMEM);
+  if (e != cudaSuccess) return e;
+  if (ev) cudaEventRecord(ev[3], st);   // the combine is fused into the up-projection
+  const unsigned nblk = (unsigned)(((long long)a.B * a.N + UP_NR - 1) / UP_NR);
+  combine_uproj_tc_kernel<<<dim3(a.H, nblk), kThreads, UP_SMEM, st>>>(tw, a);
+  if (ev) cudaEventRecord(ev[4], st);
+  return cudaGetLastError();
+}
+
+}  // namespace kdtv

@@ -1,0 +1,14 @@
+// TMA tensor-map helper shared by the tensor-core translation units.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace kdtv {
+
+// 2-D bf16 tensor map, 128-byte swizzle: a rows x cols view with a row stride
+// of row_stride_elems elements (0 = cols), boxes of box_rows x box_cols.
+CUresult encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_cols, uint32_t box_rows, uint64_t row_stride_elems = 0);
+
+}  // namespace kdtv

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(HERE, "libkdtv.so")
 
 KDTV_F32, KDTV_BF16 = 0, 1
 KDTV_FLAG_SIMT = 0x1
+KDTV_FLAG_SIMT_PROJ = 0x2
 KDTV_FLAG_TEST_STALL = 0x100
 STATUS = {0: "KDTV_OK", 1: "KDTV_ERR_INVALID_ARG", 2: "KDTV_ERR_UNSUPPORTED",
           3: "KDTV_ERR_CUDA", 4: "KDTV_ERR_BAD_TREE", 5: "KDTV_ERR_DEVICE_TIMEOUT",
@@ -24,7 +25,8 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 # Every symbol include/kdtv.h declares (checked by the CPU tests).
 EXPORTS = ("kdtv_workspace_size", "kdtv_verify_attn", "kdtv_get_device_status",
-           "kdtv_strerror", "kdtv_launches_per_call")
+           "kdtv_strerror", "kdtv_launches_per_call", "kdtv_tree_accept", "kdtv_compact_kv",
+           "kdtv_tree_build")
 
 
 class KdtvDims(ctypes.Structure):
@@ -70,6 +72,13 @@ def lib():
         L.kdtv_strerror.restype = ctypes.c_char_p
         L.kdtv_launches_per_call.argtypes = [P]
         L.kdtv_launches_per_call.restype = ctypes.c_int
+        i32 = ctypes.c_int
+        L.kdtv_tree_accept.argtypes = [i32, i32] + [vp] * 6 + [vp]
+        L.kdtv_tree_accept.restype = ctypes.c_int
+        L.kdtv_compact_kv.argtypes = [P] + [vp] * 7 + [vp]
+        L.kdtv_compact_kv.restype = ctypes.c_int
+        L.kdtv_tree_build.argtypes = [i32, i32, i32, i32] + [vp] * 8 + [vp]
+        L.kdtv_tree_build.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -183,3 +192,61 @@ def for_workload(wl, device="cuda", **kw):
 
 def default_scale(d_nope, d_rope):
     return 1.0 / math.sqrt(d_nope + d_rope)
+
+
+def _p(t):
+    return t.data_ptr() if t is not None else None
+
+
+def _s(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def tree_accept(parent, draft_tok, target_argmax, stream=None):
+    """Torch caller of kdtv_tree_accept; returns (path, path_len, bonus)."""
+    import torch
+    B, N = parent.shape
+    dev = parent.device
+    path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    plen = torch.empty(B, dtype=torch.int32, device=dev)
+    bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    code = lib().kdtv_tree_accept(B, N, _p(parent), _p(draft_tok), _p(target_argmax),
+                                  _p(path), _p(plen), _p(bonus), _s(stream))
+    if code:
+        raise KdtvError(code, "kdtv_tree_accept")
+    return path, plen, bonus
+
+
+def compact_kv(dims, c_kv, k_rope, prefix_len, path, path_len, page_table=None,
+               status=None, stream=None):
+    """Torch caller of kdtv_compact_kv (in place); returns the status tensor."""
+    import torch
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=c_kv.device)
+    code = lib().kdtv_compact_kv(ctypes.byref(dims), _p(c_kv), _p(k_rope), _p(prefix_len),
+                                 _p(path), _p(path_len), _p(page_table), _p(status),
+                                 _s(stream))
+    if code:
+        raise KdtvError(code, "kdtv_compact_kv")
+    return status
+
+
+def tree_build(logp, tokens, root_token, n_nodes, stream=None):
+    """Torch caller of kdtv_tree_build; returns dict(parent, token, depth,
+    score, n_nodes)."""
+    import torch
+    B, D, K = logp.shape
+    dev = logp.device
+    N = n_nodes
+    out = {k: torch.empty((B, N), dtype=torch.int32, device=dev)
+           for k in ("parent", "token", "depth")}
+    out["score"] = torch.empty((B, N), dtype=torch.float32, device=dev)
+    out["n_nodes"] = torch.empty(B, dtype=torch.int32, device=dev)
+    code = lib().kdtv_tree_build(B, D, K, N, _p(logp), _p(tokens), _p(root_token),
+                                 _p(out["parent"]), _p(out["token"]), _p(out["depth"]),
+                                 _p(out["score"]), _p(out["n_nodes"]), _s(stream))
+    if code:
+        raise KdtvError(code, "kdtv_tree_build")
+    return out

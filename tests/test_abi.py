@@ -119,3 +119,15 @@ def test_product_path_does_not_import_oracle():
                 txt = open(os.path.join(dp, f)).read()
                 assert not re.search(r"^\s*(from|import)\s+oracle\b", txt, re.M), f
                 assert "mla_tree_attn" not in txt, f
+
+
+def test_next_steps_reject_bad_args_on_host(L):
+    fake = 256
+    assert kdtv.STATUS[L.kdtv_tree_accept(0, 8, fake, fake, fake, fake, fake, fake, None)] == "KDTV_ERR_INVALID_ARG"
+    assert kdtv.STATUS[L.kdtv_tree_accept(2, 129, fake, fake, fake, fake, fake, fake, None)] == "KDTV_ERR_UNSUPPORTED"
+    assert kdtv.STATUS[L.kdtv_tree_accept(2, 8, None, fake, fake, fake, fake, fake, None)] == "KDTV_ERR_INVALID_ARG"
+    assert kdtv.STATUS[L.kdtv_tree_build(2, 4, 65, 8, fake, fake, fake, fake, fake, fake, fake, fake, None)] == "KDTV_ERR_UNSUPPORTED"
+    assert kdtv.STATUS[L.kdtv_tree_build(2, 4, 4, 0, fake, fake, fake, fake, fake, fake, fake, fake, None)] == "KDTV_ERR_INVALID_ARG"
+    d = _dims()
+    assert kdtv.STATUS[L.kdtv_compact_kv(ctypes.byref(d), fake, fake, fake, fake, fake, None, None, None)] == "KDTV_ERR_INVALID_ARG"
+    assert kdtv.STATUS[L.kdtv_compact_kv(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, None)] == "KDTV_ERR_INVALID_ARG"
