@@ -153,7 +153,12 @@ class VerifyAttn:
             self.dims.phase_events = None
             self._ev = None
             return
+        for e in events:             # torch creates the CUDA event lazily
+            if not e.cuda_event:
+                e.record()
         handles = (ctypes.c_void_p * 5)(*[e.cuda_event for e in events])
+        if not all(handles):
+            raise RuntimeError("phase events could not be created")
         self._ev = handles
         self.dims.phase_events = ctypes.cast(handles, ctypes.c_void_p)
 
