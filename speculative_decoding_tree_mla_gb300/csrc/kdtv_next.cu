@@ -265,7 +265,8 @@ extern "C" int kdtv_tree_build(int B, int D, int K, int N, const float* logp,
                                int32_t* n_nodes, cudaStream_t stream) {
   if (B <= 0 || D < 0 || K <= 0 || N <= 0) return KDTV_ERR_INVALID_ARG;
   if (N > kMaxNodes || K > 64 || D > 4096) return KDTV_ERR_UNSUPPORTED;
-  if (!logp || !tokens || !root_token || !parent || !token || !depth || !score || !n_nodes)
+  if ((D > 0 && (!logp || !tokens)) || !root_token || !parent || !token || !depth || !score ||
+      !n_nodes)
     return KDTV_ERR_INVALID_ARG;
   const size_t sm = (size_t)N * K * (sizeof(float) + sizeof(int)) + (size_t)N * 8;
   if (sm > 48 * 1024 &&

@@ -11,23 +11,28 @@
 // fastest, so one tile holds 128/H nodes; every row of a node shares that
 // node's ancestor mask.  An item runs on a CLUSTER OF TWO CTAs that split
 // the latent dimension:
-//   CTA 0 holds q_lat[:, 0:256] + q_rope and the matching cache columns
-//         c_kv[:, 0:256] + k_rope;
-//   CTA 1 holds q_lat[:, 256:512] and c_kv[:, 256:512].
-// Each CTA computes a partial score tile S_c = Q_c K_c^T (tcgen05, TMEM),
+//   CTA 0 holds q_lat[:, 0:256] and q_rope, and reads c_kv[:, 0:256] + k_rope;
+//   CTA 1 holds q_lat[:, 256:512] and reads c_kv[:, 256:512].
+// Each CTA computes a partial score tile S_c = Q_c K_c^T on tcgen05 into TMEM,
 // the two partials are exchanged through distributed shared memory and
 // summed, both CTAs run the same online softmax on S = S_0 + S_1 (so they
-// agree bit for bit), and each accumulates its own half of the latent
-// output O_c += P . c_kv[:, 256c : 256c+256] in TMEM.  This keeps the 128-row
-// O accumulator at 256 TMEM columns per SM, next to two 64-column score
-// buffers, and the resident Q at 80 KB of shared memory per CTA.
+// agree bit for bit), and each accumulates its own half of the latent output
+// O_c += P . c_kv[:, 256c : 256c+256] in TMEM.
+//
+// TMEM (512 columns per CTA): O_c [0, 256) fp32; q_lat half [256, 384) as
+// bf16 pairs (the A operand of Q.K^T); two score buffers [384, 448) and
+// [448, 512) whose first 32 columns receive P as bf16 pairs once the scores
+// have been read (the A operand of P.V).  Shared memory: a 4-stage TMA ring
+// of 64-key cache tiles (128-byte swizzled 64-column chunks; the same tile is
+// the K-major B operand of Q.K^T and the MN-major B operand of P.V), q_rope
+// (CTA 0), and the receive buffer of the score exchange.
 //
 // Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs, warps 2-5 (one thread per query row / TMEM lane) do the
-// score exchange, masking, softmax, P stores and the epilogue.  Every wait is
-// bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL); on timeout the kernel
-// records KDTV_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs,
-// frees TMEM and returns.
+// issues the MMAs, warps 2-5 (one thread per query row / TMEM lane) load Q
+// into TMEM, exchange scores, mask, run the softmax, write P and the
+// epilogue.  Every wait is bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL);
+// on timeout the kernel records KDTV_ERR_DEVICE_TIMEOUT, drains its in-flight
+// copies and MMAs, frees TMEM and returns.
 
 #include <cuda.h>
 
@@ -44,44 +49,53 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 64;           // keys per tile (MMA N of Q.K^T)
 constexpr int CH = 64;           // bf16 columns per 128-byte swizzled chunk
 constexpr int kHalf = 256;       // latent columns per CTA
-constexpr int kStages = 2;
-constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk
-constexpr int kQChunk = BM * CH * 2;   // 16 KiB
-constexpr int kKVChunk = BN * CH * 2;  // 8 KiB
+constexpr int kStages = 4;
+constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk per key tile
+constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
+constexpr int kQRopeBytes = BM * CH * 2;
 constexpr int kRxStride = 68;    // floats per exchanged score row (64 + pad)
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr int kColO = 0;         // O_c: columns [0, 256)
-constexpr int kColS = 256;       // score buffers: [256, 320), [320, 384)
+constexpr int kColO = 0;
+constexpr int kColQ = 256;
+constexpr int kColSP = 384;      // + 64 * buffer
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + kMaxCh * kQChunk;
-constexpr int OFF_P = OFF_KV + kStages * kMaxCh * kKVChunk;
-constexpr int OFF_RX = OFF_P + BM * CH * 2;
+constexpr int OFF_KV = 0;
+constexpr int OFF_QR = OFF_KV + kStages * kMaxCh * kKVChunk;
+constexpr int OFF_RX = OFF_QR + kQRopeBytes;
 constexpr int OFF_ANC = OFF_RX + BM * kRxStride * 4;
 constexpr int OFF_BAR = OFF_ANC + kMaxNodes * 16;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 24;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
 
 enum Bar {
-  B_Q_FULL = 0, B_KV_FULL = 1, B_KV_EMPTY = 3, B_S_FULL = 5, B_S_EMPTY = 7,
-  B_P_FULL = 9, B_P_EMPTY = 10, B_O_FULL = 11, B_RX_FULL = 12, B_TX_OK = 13,
-  B_STALL = 14, B_MMA_DONE = 15
+  B_QR_FULL = 0, B_Q_READY = 1, B_KV_FULL = 2, B_KV_EMPTY = 6, B_S_FULL = 10, B_P_FULL = 12,
+  B_P_EMPTY = 14, B_O_FULL = 16, B_RX_FULL = 17, B_TX_OK = 18, B_STALL = 19, B_MMA_DONE = 20
 };
 
 // Wait sites (reported as the timeout detail).
-enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_S_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK,
-            W_RX_FULL, W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN };
+enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK, W_RX_FULL,
+            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN };
 
 struct TcCfg {
   int row_tiles;               // ceil(N * H / 128)
   unsigned long long limit_ns; // bound on every wait
 };
 
+__device__ __forceinline__ float max64(const float (&v)[64]) {
+  float m[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
-               const __grid_constant__ CUtensorMap tm_qrope,
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                const __grid_constant__ CUtensorMap tm_ckv,
                const __grid_constant__ CUtensorMap tm_krope, const Args a, const TcCfg cfg) {
   extern __shared__ uint8_t smem_raw[];
@@ -104,18 +118,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
 
   // ---- prologue: barriers, validation, ancestor masks, TMEM ------------------------
   if (tid == 0) {
-    mbar_init(BAR(B_Q_FULL), 1);
+    mbar_init(BAR(B_QR_FULL), 1);
+    mbar_init(BAR(B_Q_READY), 4);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(BAR(B_KV_FULL + i), 1);
       mbar_init(BAR(B_KV_EMPTY + i), 1);
-      mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_S_EMPTY + i), 128);
     }
-    mbar_init(BAR(B_P_FULL), 128);
-    mbar_init(BAR(B_P_EMPTY), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(BAR(B_S_FULL + i), 1);
+      mbar_init(BAR(B_P_FULL + i), 4);
+      mbar_init(BAR(B_P_EMPTY + i), 1);
+    }
     mbar_init(BAR(B_O_FULL), 1);
-    mbar_init(BAR(B_RX_FULL), 128);
-    mbar_init(BAR(B_TX_OK), 128);
+    mbar_init(BAR(B_RX_FULL), 4);
+    mbar_init(BAR(B_TX_OK), 4);
     mbar_init(BAR(B_STALL), 1);
     mbar_init(BAR(B_MMA_DONE), 1);
     fence_mbar_init();
@@ -166,20 +182,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
   if (warp == 0) {
     // ---- TMA producer --------------------------------------------------------------
     if (lane == 0 && nt > 0) {
-      prefetch_tmap(&tm_qlat);
       prefetch_tmap(&tm_ckv);
       const int qrow = (int)(req_row0 + (long long)rt * BM);
-      mbar_expect_tx(BAR(B_Q_FULL), nch * kQChunk);
-      for (int c = 0; c < 4; ++c)
-        tma_load_2d(sbase + OFF_Q + c * kQChunk, &tm_qlat, BAR(B_Q_FULL),
-                    (int)rank * kHalf + c * CH, qrow);
-      if (rank == 0)
-        tma_load_2d(sbase + OFF_Q + 4 * kQChunk, &tm_qrope, BAR(B_Q_FULL), 0, qrow);
+      if (rank == 0) {
+        mbar_expect_tx(BAR(B_QR_FULL), kQRopeBytes);
+        tma_load_2d(sbase + OFF_QR, &tm_qrope, BAR(B_QR_FULL), 0, qrow);
+      }
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
-        const int stg = j & 1;
+        const int stg = j & (kStages - 1);
         if (j >= kStages &&
-            !wait(BAR(B_KV_EMPTY + stg), ((j >> 1) - 1) & 1, st, limit, W_KV_EMPTY))
+            !wait(BAR(B_KV_EMPTY + stg), ((j / kStages) - 1) & 1, st, limit, W_KV_EMPTY))
           break;
         const int t0 = k0 + j * BN;
         int row;
@@ -197,9 +210,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
         issued = j + 1;
       }
       // Drain: every issued copy has landed before this CTA may exit.
-      wait(BAR(B_Q_FULL), 0, st, limit, W_DRAIN);
+      if (rank == 0) wait(BAR(B_QR_FULL), 0, st, limit, W_DRAIN);
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-        wait(BAR(B_KV_FULL + (j & 1)), (j >> 1) & 1, st, limit, W_DRAIN);
+        wait(BAR(B_KV_FULL + (j & (kStages - 1))), (j / kStages) & 1, st, limit, W_DRAIN);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -207,43 +220,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
     if (lane == 0 && nt > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
-      bool alive = wait(BAR(B_Q_FULL), 0, st, limit, W_Q);
+      bool alive = wait(BAR(B_Q_READY), 0, st, limit, W_Q);
+      if (alive && rank == 0) alive = wait(BAR(B_QR_FULL), 0, st, limit, W_Q);
       for (int j = 0; alive && j <= nt; ++j) {
         if (j < nt) {
-          const int stg = j & 1;
-          alive = wait(BAR(B_KV_FULL + stg), (j >> 1) & 1, st, limit, W_KV_FULL);
-          if (alive && j >= kStages)
-            alive = wait(BAR(B_S_EMPTY + stg), ((j >> 1) - 1) & 1, st, limit, W_S_EMPTY);
+          const int stg = j & (kStages - 1), buf = j & 1;
+          alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
           if (!alive) break;
           tc_fence_after();
-          const uint32_t d = tmem + kColS + stg * BN;
+          const uint32_t d = tmem + kColSP + 64 * buf;
           const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
-          for (int c = 0; c < nch; ++c) {
 #pragma unroll
-            for (int kk = 0; kk < CH / 16; ++kk) {
-              uint64_t ad = smem_desc(sbase + OFF_Q + c * kQChunk + kk * 32, 16, 1024);
-              uint64_t bd = smem_desc(kv + c * kKVChunk + kk * 32, 16, 1024);
-              mma_bf16(d, ad, bd, kIdescQK, (c | kk) != 0);
+          for (int kk = 0; kk < kHalf / 16; ++kk) {     // latent half: A = q_lat in TMEM
+            uint64_t bd = smem_desc(kv + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ts(d, tmem + kColQ + 8 * kk, bd, kIdescQK, kk > 0);
+          }
+          if (rank == 0) {
+#pragma unroll
+            for (int kk = 0; kk < CH / 16; ++kk) {      // rope: A = q_rope in smem
+              uint64_t ad = smem_desc(sbase + OFF_QR + kk * 32, 16, 1024);
+              uint64_t bd = smem_desc(kv + 4 * kKVChunk + kk * 32, 16, 1024);
+              mma_bf16(d, ad, bd, kIdescQK, 1);
             }
           }
-          mma_commit(BAR(B_S_FULL + stg));
+          mma_commit(BAR(B_S_FULL + buf));
         }
         if (j >= 1) {
-          const int jj = j - 1, stg = jj & 1;
-          alive = wait(BAR(B_P_FULL), jj & 1, st, limit, W_P_FULL);
+          const int jj = j - 1, stg = jj & (kStages - 1), buf = jj & 1;
+          alive = wait(BAR(B_P_FULL + buf), (jj >> 1) & 1, st, limit, W_P_FULL);
           if (!alive) break;
           tc_fence_after();
           const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
-            uint64_t ad = smem_desc(sbase + OFF_P + kk * 32, 16, 1024);
             // V = c_kv columns of this CTA, MN-major: 64-column chunks are
             // kKVChunk apart (LBO), 8-key groups 1024 B apart (SBO).
             uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
-            mma_bf16(tmem + kColO, ad, bd, kIdescPV, (jj > 0 || kk > 0));
+            mma_bf16_ts(tmem + kColO, tmem + kColSP + 64 * buf + 8 * kk, bd, kIdescPV,
+                        (jj > 0 || kk > 0));
           }
           mma_commit(BAR(B_KV_EMPTY + stg));
-          mma_commit(BAR(B_P_EMPTY));
+          mma_commit(BAR(B_P_EMPTY + buf));
         }
       }
       if (alive) mma_commit(BAR(B_O_FULL));
@@ -252,17 +269,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
     }
     __syncwarp();
   } else {
-    // ---- softmax / exchange / epilogue (warps 2..5) ----------------------------------
+    // ---- Q load, score exchange, softmax, P, epilogue (warps 2..5) --------------------
     const int q = warp & 3;                      // TMEM lane quadrant of this warp
     const int r = q * 32 + lane;                 // row within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const int rr = rt * BM + r;                  // row within the request
     const bool row_valid = rr < a.N * a.H;
     const int node = row_valid ? rr / a.H : 0;
-    uint32_t my_anc[4] = {0u, 0u, 0u, 0u};
+    uint32_t an0 = 0, an1 = 0, an2 = 0, an3 = 0;
     if (ok && row_valid) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) my_anc[w] = anc[4 * node + w];
+      an0 = anc[4 * node]; an1 = anc[4 * node + 1]; an2 = anc[4 * node + 2]; an3 = anc[4 * node + 3];
     }
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
     float m_used = -INFINITY, l_sum = 0.f;
@@ -271,29 +287,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
     const uint32_t rx_remote = mapa(rx_local, peer);
     const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL), peer);
     const uint32_t txok_remote = mapa(BAR(B_TX_OK), peer);
-    const uint32_t p_row = sbase + OFF_P + r * 128;
 
-    if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL)) {
-      alive = wait(BAR(B_STALL), 0, st, limit, W_STALL);   // nothing arrives here
-      alive = __all_sync(0xffffffffu, alive);
+    if (nt > 0) {
+      // q_lat half of this row -> TMEM columns [kColQ, kColQ + 128) as bf16 pairs.
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(a.q_lat) + (req_row0 + (row_valid ? rr : 0)) * 512 +
+          rank * kHalf);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint4 x = row_valid ? src[8 * c + v] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+        }
+        tmem_st32u(tmem + lane_addr + kColQ + 32 * c, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_Q_READY));
     }
 
+    if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL))
+      alive = __all_sync(0xffffffffu, wait(BAR(B_STALL), 0, st, limit, W_STALL));
+
     for (int j = 0; alive && j < nt; ++j) {
-      const int stg = j & 1;
-      alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + stg), (j >> 1) & 1, st, limit, W_S_FULL));
+      const int buf = j & 1;
+      alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
       if (!alive) break;
       tc_fence_after();
       float sv[64];
       {
         float t0v[32], t1v[32];
-        tmem_ld32(tmem + lane_addr + kColS + stg * BN, t0v);
-        tmem_ld32(tmem + lane_addr + kColS + stg * BN + 32, t1v);
+        tmem_ld32(tmem + lane_addr + kColSP + 64 * buf, t0v);
+        tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32, t1v);
         tmem_wait_ld();
 #pragma unroll
         for (int k = 0; k < 32; ++k) { sv[k] = t0v[k]; sv[32 + k] = t1v[k]; }
       }
-      tc_fence_before();
-      mbar_arrive(BAR(B_S_EMPTY + stg));
 
       // exchange the partial scores with the peer CTA
       if (j >= 1) {
@@ -306,7 +338,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                      :: "r"(rx_remote + 16 * v), "f"(sv[4 * v]), "f"(sv[4 * v + 1]),
                         "f"(sv[4 * v + 2]), "f"(sv[4 * v + 3]) : "memory");
       }
-      mbar_arrive_remote(rxfull_remote);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(rxfull_remote);
       alive = __all_sync(0xffffffffu, wait<true>(BAR(B_RX_FULL), j & 1, st, limit, W_RX_FULL));
       if (!alive) break;
 #pragma unroll
@@ -317,54 +350,65 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
                      : "memory");
         sv[4 * v] += x0; sv[4 * v + 1] += x1; sv[4 * v + 2] += x2; sv[4 * v + 3] += x3;
       }
-      mbar_arrive_remote(txok_remote);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(txok_remote);
 
-      // visibility mask, scale, tile max
+      // visibility mask (only tiles that reach past the prefix), tile max
       const int t0 = k0 + j * BN;
-      float m_tile = -INFINITY;
-      if (row_valid && t0 + BN <= L) {
-#pragma unroll
-        for (int k = 0; k < BN; ++k) { sv[k] *= sl2; m_tile = fmaxf(m_tile, sv[k]); }
-      } else {
+      if (!(row_valid && t0 + BN <= L)) {
 #pragma unroll
         for (int k = 0; k < BN; ++k) {
           const int t = t0 + k;
           bool vis = false;
           if (row_valid && t < k1) {
-            if (t < L) vis = true;
-            else { const int jn = t - L; vis = (my_anc[jn >> 5] >> (jn & 31)) & 1u; }
+            if (t < L) {
+              vis = true;
+            } else {
+              const int jn = t - L;
+              const uint32_t w = jn < 32 ? an0 : jn < 64 ? an1 : jn < 96 ? an2 : an3;
+              vis = (w >> (jn & 31)) & 1u;
+            }
           }
-          sv[k] = vis ? sv[k] * sl2 : -INFINITY;
-          m_tile = fmaxf(m_tile, sv[k]);
+          if (!vis) sv[k] = -INFINITY;
         }
       }
+      const float m_tile = max64(sv) * sl2;
+
       // lazy rescale: move the reference max only when it grows by > 8 (log2)
       float alpha = 1.f;
       bool rescale = false;
       if (m_tile > m_used + 8.f) {
-        if (m_used != -INFINITY) { alpha = exp2f(m_used - m_tile); rescale = true; }
+        if (m_used != -INFINITY) { alpha = ex2(m_used - m_tile); rescale = true; }
         l_sum *= alpha;
         m_used = m_tile;
       }
+      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
       uint32_t packed[32];
-      float psum = 0.f;
+      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < BN; k += 2) {
-        float p0 = (sv[k] == -INFINITY) ? 0.f : exp2f(sv[k] - m_used);
-        float p1 = (sv[k + 1] == -INFINITY) ? 0.f : exp2f(sv[k + 1] - m_used);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        psum += __low2float(h2) + __high2float(h2);
-        packed[k >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+        const float p0 = ex2(fmaf(sv[k], sl2, neg_m));
+        const float p1 = ex2(fmaf(sv[k + 1], sl2, neg_m));
+        const uint32_t h2 = pack_bf16x2(p0, p1);
+        packed[k >> 1] = h2;
+        ps[(k >> 1) & 7] += __uint_as_float(h2 << 16) + __uint_as_float(h2 & 0xffff0000u);
       }
-      l_sum += psum;
+      l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 
-      // P and O are free once the previous P.V has completed
-      if (j >= 1) {
-        alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY), (j - 1) & 1, st, limit, W_P_EMPTY));
+      // the P buffer is free once P.V of tile j-2 (same buffer) has completed;
+      // O is stable once P.V of tile j-1 has completed
+      if (j >= 2) {
+        alive = __all_sync(0xffffffffu,
+                           wait(BAR(B_P_EMPTY + buf), ((j >> 1) - 1) & 1, st, limit, W_P_EMPTY));
         if (!alive) break;
       }
-      tc_fence_after();
       if (__any_sync(0xffffffffu, rescale)) {
+        if (j >= 1) {
+          alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + (buf ^ 1)), ((j - 1) >> 1) & 1, st,
+                                               limit, W_P_EMPTY));
+          if (!alive) break;
+        }
+        tc_fence_after();
         for (int c = 0; c < kHalf / 32; ++c) {
           float ov[32];
           tmem_ld32(tmem + lane_addr + kColO + 32 * c, ov);
@@ -373,19 +417,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat,
           for (int k = 0; k < 32; ++k) ov[k] *= alpha;
           tmem_st32(tmem + lane_addr + kColO + 32 * c, ov);
         }
-        tmem_wait_st();
       }
-      // P row: 64 bf16 = eight 16-byte chunks, 128-byte swizzle (chunk ^ row%8)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = p_row + ((c ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(addr), "r"(packed[4 * c]), "r"(packed[4 * c + 1]),
-                        "r"(packed[4 * c + 2]), "r"(packed[4 * c + 3]) : "memory");
-      }
-      fence_async_smem();
+      tc_fence_after();
+      tmem_st32u(tmem + lane_addr + kColSP + 64 * buf, packed);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(BAR(B_P_FULL));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_P_FULL + buf));
     }
 
     // ---- epilogue: unnormalised partial o_lat half, (m, l) -----------------------------
@@ -510,9 +548,8 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
   const long long rows = (long long)a.B * a.N * a.H;
   const long long kv_rows = a.page_size ? (long long)a.num_pages * a.page_size
                                         : (long long)a.B * a.t_stride;
-  CUtensorMap tq, tqr, tck, tkr;
-  if (encode_2d(&tq, a.q_lat, rows, 512, CH, BM) != CUDA_SUCCESS ||
-      encode_2d(&tqr, a.q_rope, rows, 64, CH, BM) != CUDA_SUCCESS ||
+  CUtensorMap tqr, tck, tkr;
+  if (encode_2d(&tqr, a.q_rope, rows, 64, CH, BM) != CUDA_SUCCESS ||
       encode_2d(&tck, a.c_kv, kv_rows, 512, CH, BN) != CUDA_SUCCESS ||
       encode_2d(&tkr, a.k_rope, kv_rows, 64, CH, BN) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
@@ -530,7 +567,7 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
   e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<(unsigned)(2 * items), kThreads, kSmemBytes, st>>>(tq, tqr, tck, tkr, a, cfg);
+  attn_tc_kernel<<<(unsigned)(2 * items), kThreads, kSmemBytes, st>>>(tqr, tck, tkr, a, cfg);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], st);

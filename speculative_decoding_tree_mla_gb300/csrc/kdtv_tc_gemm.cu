@@ -29,9 +29,14 @@ constexpr uint64_t kLimitNs = 2000000000ull;
 // ---- A1: absorb -----------------------------------------------------------------------
 constexpr int AB_M = 128;                  // latent columns per CTA
 constexpr int AB_NR = 128;                 // query rows (b, i) per CTA
-constexpr int AB_OFF_B = 2 * 256 * 128;    // A: two MN atoms of up to 256 e-rows x 128 B
-constexpr int AB_OFF_BAR = AB_OFF_B + 4 * AB_NR * 128;
-constexpr int AB_SMEM = AB_OFF_BAR + 64 + 1024;
+
+// Shared memory of absorb_tc_kernel for a given d_nope: A = two MN atoms of
+// d_nope e-rows x 128 B, B = d_nope/64 chunks of AB_NR rows x 128 B, barriers.
+__host__ __device__ constexpr int ab_off_b(int d_nope) { return 2 * d_nope * 128; }
+__host__ __device__ constexpr int ab_off_bar(int d_nope) {
+  return ab_off_b(d_nope) + (d_nope / 64) * AB_NR * 128;
+}
+__host__ __device__ constexpr int ab_smem(int d_nope) { return ab_off_bar(d_nope) + 64 + 1024; }
 
 __global__ void __launch_bounds__(kThreads, 1)
 absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
@@ -48,15 +53,16 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int nr = min(AB_NR, BNr - r0);
   const int n_mma = (nr + 15) & ~15;
   const int kch = a.d_nope / 64;             // 64-wide K chunks
-  const uint32_t bar_full = sbase + AB_OFF_BAR, bar_mma = bar_full + 8;
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + AB_OFF_BAR + 16);
+  const int off_b = ab_off_b(a.d_nope), off_bar = ab_off_bar(a.d_nope);
+  const uint32_t bar_full = sbase + off_bar, bar_mma = bar_full + 8;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + off_bar + 16);
 
   if (tid == 0) {
     mbar_init(bar_full, 1);
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) { tmem_alloc(sbase + AB_OFF_BAR + 16, AB_NR); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(sbase + off_bar + 16, AB_NR); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -69,7 +75,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     for (int c = 0; c < 2; ++c)       // W_UK[h][:, d0 + 64c : +64]: e-rows x 64 d
       tma_load_2d(sbase + c * a.d_nope * 128, &tm_w, bar_full, d0 + 64 * c, h * a.d_nope);
     for (int k = 0; k < kch; ++k)     // q_nope rows r0.. of head h, e in [64k, 64k+64)
-      tma_load_2d(sbase + AB_OFF_B + k * AB_NR * 128, &tm_q, bar_full, h * a.d_nope + 64 * k, r0);
+      tma_load_2d(sbase + off_b + k * AB_NR * 128, &tm_q, bar_full, h * a.d_nope + 64 * k, r0);
     ok = wait(bar_full, 0, a.status, kLimitNs, 101);
     if (ok) {
       tc_fence_after();
@@ -77,7 +83,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       for (int kk = 0; kk < a.d_nope / 16; ++kk) {
         // A (MN-major): 64-column atoms a.d_nope*128 B apart, 8 e-rows per 1 KiB.
         uint64_t ad = smem_desc(sbase + kk * 16 * 128, a.d_nope * 128, 1024);
-        uint64_t bd = smem_desc(sbase + AB_OFF_B + (kk >> 2) * AB_NR * 128 + (kk & 3) * 32, 16, 1024);
+        uint64_t bd = smem_desc(sbase + off_b + (kk >> 2) * AB_NR * 128 + (kk & 3) * 32, 16, 1024);
         mma_bf16(tmem, ad, bd, idesc, kk > 0);
       }
     }
@@ -115,7 +121,10 @@ constexpr int UP_OFF_W = UP_OFF_B + 8 * UP_NR * 128;
 constexpr int UP_OFF_BAR = UP_OFF_W + UP_NR * UP_MAX_SPLITS * 4;
 constexpr int UP_SMEM = UP_OFF_BAR + 64 + 1024;
 
-__global__ void __launch_bounds__(kThreads, 1)
+constexpr int UP_THREADS = 256;   // all warps merge partials; warps 0-3 read TMEM
+constexpr int UP_BATCH = 4;       // row/8-column units merged per thread per pass
+
+__global__ void __launch_bounds__(UP_THREADS, 1)
 combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -175,34 +184,55 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   __syncthreads();
 
   // o_lat rows -> bf16, 128-byte swizzled K-major operand: row r, 8-column unit u.
-  for (int idx = tid; idx < UP_NR * 64; idx += kThreads) {
-    const int r = idx >> 6, u = idx & 63;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (r < nr) {
-      const long long grow = (long long)(r0 + r) * a.H + h;
-      const float* w = wts + r * UP_MAX_SPLITS;
-      for (int s = 0; s < S; ++s) {
-        const float ws = w[s];
-        if (ws == 0.f) continue;
-        const float4* src =
-            reinterpret_cast<const float4*>(a.part_o + ((long long)s * rows + grow) * 512 + 8 * u);
-        const float4 x0 = src[0], x1 = src[1];
-        acc[0] = fmaf(ws, x0.x, acc[0]); acc[1] = fmaf(ws, x0.y, acc[1]);
-        acc[2] = fmaf(ws, x0.z, acc[2]); acc[3] = fmaf(ws, x0.w, acc[3]);
-        acc[4] = fmaf(ws, x1.x, acc[4]); acc[5] = fmaf(ws, x1.y, acc[5]);
-        acc[6] = fmaf(ws, x1.z, acc[6]); acc[7] = fmaf(ws, x1.w, acc[7]);
+  // Each pass merges UP_BATCH units per thread with all their loads in flight.
+  for (int base = tid; base < UP_NR * 64; base += UP_THREADS * UP_BATCH) {
+    float acc[UP_BATCH][8];
+#pragma unroll
+    for (int uu = 0; uu < UP_BATCH; ++uu)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[uu][e] = 0.f;
+    for (int s = 0; s < S; ++s) {
+      float4 x[UP_BATCH][2];
+      float ws[UP_BATCH];
+#pragma unroll
+      for (int uu = 0; uu < UP_BATCH; ++uu) {
+        const int idx = base + uu * UP_THREADS;
+        const int r = idx >> 6, u = idx & 63;
+        ws[uu] = (idx < UP_NR * 64 && r < nr) ? wts[r * UP_MAX_SPLITS + s] : 0.f;
+        if (ws[uu] != 0.f) {
+          const float4* src = reinterpret_cast<const float4*>(
+              a.part_o + ((long long)s * rows + (long long)(r0 + r) * a.H + h) * 512 + 8 * u);
+          x[uu][0] = src[0];
+          x[uu][1] = src[1];
+        } else {
+          x[uu][0] = x[uu][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int uu = 0; uu < UP_BATCH; ++uu) {
+        acc[uu][0] = fmaf(ws[uu], x[uu][0].x, acc[uu][0]);
+        acc[uu][1] = fmaf(ws[uu], x[uu][0].y, acc[uu][1]);
+        acc[uu][2] = fmaf(ws[uu], x[uu][0].z, acc[uu][2]);
+        acc[uu][3] = fmaf(ws[uu], x[uu][0].w, acc[uu][3]);
+        acc[uu][4] = fmaf(ws[uu], x[uu][1].x, acc[uu][4]);
+        acc[uu][5] = fmaf(ws[uu], x[uu][1].y, acc[uu][5]);
+        acc[uu][6] = fmaf(ws[uu], x[uu][1].z, acc[uu][6]);
+        acc[uu][7] = fmaf(ws[uu], x[uu][1].w, acc[uu][7]);
       }
     }
-    uint32_t pk[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-      pk[j] = *reinterpret_cast<uint32_t*>(&h2);
+    for (int uu = 0; uu < UP_BATCH; ++uu) {
+      const int idx = base + uu * UP_THREADS;
+      if (idx >= UP_NR * 64) continue;
+      const int r = idx >> 6, u = idx & 63;
+      uint32_t pk[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) pk[j] = pack_bf16x2(acc[uu][2 * j], acc[uu][2 * j + 1]);
+      const uint32_t addr = sbase + UP_OFF_B + (u >> 3) * UP_NR * 128 + r * 128 +
+                            (((u & 7) ^ (r & 7)) << 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                   :: "r"(addr), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]) : "memory");
     }
-    const uint32_t addr = sbase + UP_OFF_B + (u >> 3) * UP_NR * 128 + r * 128 +
-                          (((u & 7) ^ (r & 7)) << 4);
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                 :: "r"(addr), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]) : "memory");
   }
   fence_async_smem();
   __syncthreads();
@@ -225,7 +255,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   ok = wait(bar_mma, 0, a.status, kLimitNs, 112) && ok;
   ok = __all_sync(0xffffffffu, ok);
   tc_fence_after();
-  if (ok) {
+  if (ok && warp < 4) {
     const int v = warp * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     for (int c0 = 0; c0 < UP_NR; c0 += 32) {
@@ -261,11 +291,12 @@ cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st) {
   if (encode_2d(&tw, a.W_UK, (uint64_t)a.H * a.d_nope, 512, 64, a.d_nope) != CUDA_SUCCESS ||
       encode_2d(&tq, a.q_nope, BNr, (uint64_t)a.H * a.d_nope, 64, AB_NR) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  const int smem = ab_smem(a.d_nope);
   cudaError_t e = cudaFuncSetAttribute(absorb_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, AB_SMEM);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(512 / AB_M, a.H, (unsigned)((BNr + AB_NR - 1) / AB_NR));
-  absorb_tc_kernel<<<grid, kThreads, AB_SMEM, st>>>(tw, tq, a);
+  absorb_tc_kernel<<<grid, kThreads, smem, st>>>(tw, tq, a);
   return cudaGetLastError();
 }
 
@@ -280,7 +311,7 @@ cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t s
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[3], st);   // the combine is fused into the up-projection
   const unsigned nblk = (unsigned)(((long long)a.B * a.N + UP_NR - 1) / UP_NR);
-  combine_uproj_tc_kernel<<<dim3(a.H, nblk), kThreads, UP_SMEM, st>>>(tw, a);
+  combine_uproj_tc_kernel<<<dim3(a.H, nblk), UP_THREADS, UP_SMEM, st>>>(tw, a);
   if (ev) cudaEventRecord(ev[4], st);
   return cudaGetLastError();
 }
