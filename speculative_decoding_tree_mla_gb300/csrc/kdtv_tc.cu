@@ -53,7 +53,9 @@ constexpr int kStages = 4;
 constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk per key tile
 constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
 constexpr int kQRopeBytes = BM * CH * 2;
-constexpr int kRxStride = 68;    // floats per exchanged score row (64 + pad)
+// Score exchange buffer, chunk-major: 16-byte chunk v of row r at (v * BM + r) * 16,
+// so a warp's store of one chunk for its 32 rows is one contiguous 512-byte block.
+constexpr int kRxBytes = BM * BN * 4;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;
@@ -63,7 +65,7 @@ constexpr int kColSP = 384;      // + 64 * buffer
 constexpr int OFF_KV = 0;
 constexpr int OFF_QR = OFF_KV + kStages * kMaxCh * kKVChunk;
 constexpr int OFF_RX = OFF_QR + kQRopeBytes;
-constexpr int OFF_ANC = OFF_RX + BM * kRxStride * 4;
+constexpr int OFF_ANC = OFF_RX + kRxBytes;
 constexpr int OFF_BAR = OFF_ANC + kMaxNodes * 16;
 constexpr int kNumBars = 24;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
@@ -283,7 +285,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
     float m_used = -INFINITY, l_sum = 0.f;
     bool alive = true;
-    const uint32_t rx_local = sbase + OFF_RX + r * kRxStride * 4;
+    const uint32_t rx_local = sbase + OFF_RX + r * 16;
     const uint32_t rx_remote = mapa(rx_local, peer);
     const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL), peer);
     const uint32_t txok_remote = mapa(BAR(B_TX_OK), peer);
@@ -335,7 +337,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
 #pragma unroll
       for (int v = 0; v < 16; ++v) {
         asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(rx_remote + 16 * v), "f"(sv[4 * v]), "f"(sv[4 * v + 1]),
+                     :: "r"(rx_remote + v * BM * 16), "f"(sv[4 * v]), "f"(sv[4 * v + 1]),
                         "f"(sv[4 * v + 2]), "f"(sv[4 * v + 3]) : "memory");
       }
       __syncwarp();
@@ -346,12 +348,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       for (int v = 0; v < 16; ++v) {
         float x0, x1, x2, x3;
         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3) : "r"(rx_local + 16 * v)
+                     : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3) : "r"(rx_local + v * BM * 16)
                      : "memory");
         sv[4 * v] += x0; sv[4 * v + 1] += x1; sv[4 * v + 2] += x2; sv[4 * v + 3] += x3;
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(txok_remote);
 
       // visibility mask (only tiles that reach past the prefix), tile max
       const int t0 = k0 + j * BN;
@@ -423,7 +423,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_P_FULL + buf));
+      if (lane == 0) {
+        mbar_arrive(BAR(B_P_FULL + buf));
+        mbar_arrive_remote(txok_remote);   // our receive buffer may be refilled
+      }
     }
 
     // ---- epilogue: unnormalised partial o_lat half, (m, l) -----------------------------
