@@ -64,6 +64,22 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                :: "r"(cluster_bar) : "memory");
 }
 
+// Relaxed arrive on a barrier of another CTA in the cluster (no release fence:
+// only for signals that order nothing but loads whose values were consumed).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
+               :: "r"(cluster_bar) : "memory");
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory; completion is
+// counted (complete_tx, 16 bytes) on that CTA's mbarrier `cluster_bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c,
+                                            float d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      :: "r"(cluster_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"

@@ -132,10 +132,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       mbar_init(BAR(B_P_EMPTY + i), 1);
     }
     mbar_init(BAR(B_O_FULL), 1);
-    mbar_init(BAR(B_RX_FULL), 4);
-    mbar_init(BAR(B_TX_OK), 4);
+    mbar_init(BAR(B_RX_FULL), 1);   // armed with expect_tx; filled by the peer's st.async
+    mbar_init(BAR(B_TX_OK), 4);     // one relaxed arrival per peer softmax warp
     mbar_init(BAR(B_STALL), 1);
     mbar_init(BAR(B_MMA_DONE), 1);
+    mbar_expect_tx(BAR(B_RX_FULL), kRxBytes);   // phase 0 of the score exchange
     fence_mbar_init();
     int L = 0;
     int ok = prefix_ok(a, b, &L) ? 1 : 0;
@@ -329,21 +330,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         for (int k = 0; k < 32; ++k) { sv[k] = t0v[k]; sv[32 + k] = t1v[k]; }
       }
 
-      // exchange the partial scores with the peer CTA
+      // exchange the partial scores with the peer CTA: asynchronous remote
+      // stores whose bytes complete the peer's RX_FULL phase (no fences)
       if (j >= 1) {
-        alive = __all_sync(0xffffffffu, wait<true>(BAR(B_TX_OK), (j - 1) & 1, st, limit, W_TX_OK));
+        alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK), (j - 1) & 1, st, limit, W_TX_OK));
         if (!alive) break;
       }
 #pragma unroll
-      for (int v = 0; v < 16; ++v) {
-        asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-                     :: "r"(rx_remote + v * BM * 16), "f"(sv[4 * v]), "f"(sv[4 * v + 1]),
-                        "f"(sv[4 * v + 2]), "f"(sv[4 * v + 3]) : "memory");
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(rxfull_remote);
+      for (int v = 0; v < 16; ++v)
+        st_async_v4(rx_remote + v * BM * 16, sv[4 * v], sv[4 * v + 1], sv[4 * v + 2],
+                    sv[4 * v + 3], rxfull_remote);
       alive = __all_sync(0xffffffffu, wait<true>(BAR(B_RX_FULL), j & 1, st, limit, W_RX_FULL));
       if (!alive) break;
+      if (r == 0 && j + 1 < nt) mbar_expect_tx(BAR(B_RX_FULL), kRxBytes);   // arm next phase
 #pragma unroll
       for (int v = 0; v < 16; ++v) {
         float x0, x1, x2, x3;
@@ -352,6 +351,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                      : "memory");
         sv[4 * v] += x0; sv[4 * v + 1] += x1; sv[4 * v + 2] += x2; sv[4 * v + 3] += x3;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote_relaxed(txok_remote);   // rx values consumed
 
       // visibility mask (only tiles that reach past the prefix), tile max
       const int t0 = k0 + j * BN;
@@ -423,10 +424,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(BAR(B_P_FULL + buf));
-        mbar_arrive_remote(txok_remote);   // our receive buffer may be refilled
-      }
+      if (lane == 0) mbar_arrive(BAR(B_P_FULL + buf));
     }
 
     // ---- epilogue: unnormalised partial o_lat half, (m, l) -----------------------------
