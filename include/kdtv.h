@@ -209,6 +209,41 @@ int kdtv_tree_build(int B, int D, int K, int N, const float* logp, const int32_t
                     const int32_t* root_token, int32_t* parent, int32_t* token,
                     int32_t* depth, float* score, int32_t* n_nodes, cudaStream_t stream);
 
+/* ---- allocation-free variant ----------------------------------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers of
+ * this library that cannot call cudaMalloc where they run the attention (code
+ * inside an arena or pool allocator that owns all device memory, server
+ * plugins that may only touch pre-registered buffers, or processes that
+ * forbid device allocation after start-up).
+ *
+ * kdtv_verify_attn_noalloc computes exactly what kdtv_verify_attn computes,
+ * with the same arguments, but takes its scratch from a fixed array of
+ * KDTV_NOALLOC_SCRATCH_BYTES that lives in this library's device image
+ * (dims->workspace and dims->workspace_bytes are ignored).  It allocates
+ * nothing.  Every GPU that loads the library holds that array until the
+ * process exits.
+ *   - Returns KDTV_ERR_UNSUPPORTED, before any launch, if the call needs more
+ *     scratch than KDTV_NOALLOC_SCRATCH_BYTES (kdtv_workspace_size(dims) larger
+ *     than the array); other errors as kdtv_verify_attn.
+ *   - status_out: device pointer to one unsigned int; when the call's kernels
+ *     have finished it holds the call's device status (KDTV_OK or a device-side
+ *     KDTV_ERR_* as kdtv_get_device_status would report).  Asynchronous on
+ *     `stream` like every other entry point.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture on that device.
+ *   - All calls share the one array per device: calls that may overlap on the
+ *     GPU (different streams or host threads) race and must be serialised by
+ *     the caller.
+ */
+#define KDTV_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+int kdtv_verify_attn_noalloc(const kdtv_dims* dims, const void* q_nope, const void* q_rope,
+                             const void* W_UK, const void* W_UV, const void* c_kv,
+                             const void* k_rope, const int32_t* parent,
+                             const int32_t* prefix_len, const int32_t* page_table,
+                             float* out, unsigned int* status_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

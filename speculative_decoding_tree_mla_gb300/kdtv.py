@@ -26,7 +26,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 # Every symbol include/kdtv.h declares (checked by the CPU tests).
 EXPORTS = ("kdtv_workspace_size", "kdtv_verify_attn", "kdtv_get_device_status",
            "kdtv_strerror", "kdtv_launches_per_call", "kdtv_tree_accept", "kdtv_compact_kv",
-           "kdtv_tree_build")
+           "kdtv_tree_build", "kdtv_verify_attn_noalloc")
 
 
 class KdtvDims(ctypes.Structure):
@@ -79,6 +79,8 @@ def lib():
         L.kdtv_compact_kv.restype = ctypes.c_int
         L.kdtv_tree_build.argtypes = [i32, i32, i32, i32] + [vp] * 8 + [vp]
         L.kdtv_tree_build.restype = ctypes.c_int
+        L.kdtv_verify_attn_noalloc.argtypes = [P] + [vp] * 11 + [vp]
+        L.kdtv_verify_attn_noalloc.restype = ctypes.c_int
         _lib = L
     return _lib
 
