@@ -106,6 +106,28 @@ __device__ __forceinline__ bool ancestor_mask(const Args& a, int b, int i,
   return false;
 }
 
+// Same walk over a copy of parent[b][0 .. N) already in shared memory.
+__device__ __forceinline__ bool ancestor_mask_smem(const Args& a, int b, const int32_t* par, int i,
+                                                   uint32_t mask[4]) {
+  mask[0] = mask[1] = mask[2] = mask[3] = 0u;
+  if (par[0] != -1) {
+    record_error(a.status, KDTV_ERR_BAD_TREE, (unsigned)b);
+    return false;
+  }
+  int j = i;
+  for (int step = 0; step <= a.N; ++step) {
+    mask[j >> 5] |= 1u << (j & 31);
+    if (j == 0) return true;
+    int p = par[j];
+    if (p < 0 || p >= j) {
+      record_error(a.status, KDTV_ERR_BAD_TREE, (unsigned)(b * 65536 + j));
+      return false;
+    }
+    j = p;
+  }
+  return false;
+}
+
 __device__ __forceinline__ bool prefix_ok(const Args& a, int b, int* L) {
   int l = a.prefix_len[b];
   int cap = a.page_size ? a.max_pages * a.page_size : a.t_stride;
@@ -115,6 +137,25 @@ __device__ __forceinline__ bool prefix_ok(const Args& a, int b, int* L) {
   }
   *L = l;
   return true;
+}
+
+// Launch with an optional programmatic-dependent-launch attribute: the kernel
+// may begin while the previous kernel of the stream drains, and must call
+// griddepcontrol.wait before touching that kernel's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 // Launchers (one per translation unit).

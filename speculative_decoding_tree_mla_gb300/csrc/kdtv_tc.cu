@@ -25,16 +25,19 @@
 // have been read (the A operand of P.V).  Shared memory: a 4-stage TMA ring
 // of 64-key cache tiles (128-byte swizzled 64-column chunks; the same tile is
 // the K-major B operand of Q.K^T and the MN-major B operand of P.V), q_rope
-// (CTA 0), and the receive buffer of the score exchange.
+// (CTA 0), and two receive buffers of the score exchange.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs, warps 2-5 (one thread per query row / TMEM lane) load Q
-// into TMEM, exchange scores, mask, run the softmax, write P and the
-// epilogue.  Every wait is bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL);
+// Warp roles (448 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
+// issues the MMAs; warps 2-5 (one thread per query row / TMEM lane) read each
+// partial score tile and stream it to the peer with st.async as scaled fp16;
+// warps 6-13 (two threads per row, 32 key columns each) load Q into TMEM, add
+// the peer's partial, mask, run the softmax, write P and the epilogue.  Two
+// receive buffers let the transfer of tile j+1 overlap the softmax of tile j.  Every wait is bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL);
 // on timeout the kernel records KDTV_ERR_DEVICE_TIMEOUT, drains its in-flight
 // copies and MMAs, frees TMEM and returns.
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "kdtv_internal.cuh"
 #include "kdtv_ptx.cuh"
@@ -53,10 +56,15 @@ constexpr int kStages = 4;
 constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk per key tile
 constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
 constexpr int kQRopeBytes = BM * CH * 2;
-// Score exchange buffer, chunk-major: 16-byte chunk v of row r at (v * BM + r) * 16,
-// so a warp's store of one chunk for its 32 rows is one contiguous 512-byte block.
-constexpr int kRxBytes = BM * BN * 4;
-constexpr int kThreads = 192;
+// Score exchange buffers.  A partial score row travels as 64 fp16 values,
+// each 32-column half scaled by an exact power of two chosen from that half's
+// largest magnitude (so it cannot overflow and keeps 11 significant bits
+// relative to that maximum), plus the two 32-bit exponents.  Chunk-major:
+// 16-byte chunk v of row r at (v * BM + r) * 16, so one warp store is a
+// contiguous 512-byte block; the exponents follow as [2][BM] words.
+constexpr int kRxData = BM * BN * 2;
+constexpr int kRxBytes = kRxData + 2 * BM * 4;
+constexpr int kThreads = 448;    // TMA, MMA, 4 sender warps, 8 softmax warps (2 per row)
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;
 constexpr int kColQ = 256;
@@ -64,33 +72,62 @@ constexpr int kColSP = 384;      // + 64 * buffer
 
 constexpr int OFF_KV = 0;
 constexpr int OFF_QR = OFF_KV + kStages * kMaxCh * kKVChunk;
-constexpr int OFF_RX = OFF_QR + kQRopeBytes;
-constexpr int OFF_ANC = OFF_RX + kRxBytes;
-constexpr int OFF_BAR = OFF_ANC + kMaxNodes * 16;
-constexpr int kNumBars = 24;
+constexpr int kRxStride = (kRxBytes + 1023) / 1024 * 1024;
+constexpr int OFF_RX = OFF_QR + kQRopeBytes;                 // two receive buffers
+constexpr int OFF_ANC = OFF_RX + 2 * kRxStride;
+constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 16;               // staged parent[]
+constexpr int OFF_HMAX = OFF_PAR + kMaxNodes * 4;               // [2 tiles][2 halves][BM] floats
+constexpr int OFF_LSUM = OFF_HMAX + 2 * 2 * BM * 4;             // [2 halves][BM] floats
+constexpr int OFF_BAR = OFF_LSUM + 2 * BM * 4;
+constexpr int kNumBars = 32;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
 
-enum Bar {
-  B_QR_FULL = 0, B_Q_READY = 1, B_KV_FULL = 2, B_KV_EMPTY = 6, B_S_FULL = 10, B_P_FULL = 12,
-  B_P_EMPTY = 14, B_O_FULL = 16, B_RX_FULL = 17, B_TX_OK = 18, B_STALL = 19, B_MMA_DONE = 20
+// Barrier indices (derived from kStages so the groups never overlap).
+enum Bar : int {
+  B_QR_FULL = 0, B_Q_READY = 1, B_KV_FULL = 2,
+  B_KV_EMPTY = B_KV_FULL + kStages,
+  B_S_FULL = B_KV_EMPTY + kStages,   // [2]
+  B_S_SENT = B_S_FULL + 2,           // [2]
+  B_P_FULL = B_S_SENT + 2,           // [2]
+  B_P_EMPTY = B_P_FULL + 2,          // [2]
+  B_O_FULL = B_P_EMPTY + 2,
+  B_RX_FULL = B_O_FULL + 1,          // [2]
+  B_TX_OK = B_RX_FULL + 2,           // [2]
+  B_STALL = B_TX_OK + 2,
+  B_MMA_DONE = B_STALL + 1,
+  B_HMAX = B_MMA_DONE + 1,           // [2] the two half-row threads met (tile max)
+  B_LSUM = B_HMAX + 2,               // the two half-row threads met (row sums)
+  B_COUNT = B_LSUM + 1
 };
+static_assert(B_COUNT <= kNumBars, "barrier slots");
 
 // Wait sites (reported as the timeout detail).
 enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK, W_RX_FULL,
-            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN };
+            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_SENT };
 
 struct TcCfg {
   int row_tiles;               // ceil(N * H / 128)
   unsigned long long limit_ns; // bound on every wait
 };
 
-__device__ __forceinline__ float max64(const float (&v)[64]) {
-  float m[32];
+// 2^e as a float for e in [-126, 127] (exact).
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Shift that maps max |v| into [2^14, 2^15): the fp16 range with headroom.
+__device__ __forceinline__ int fp16_shift(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;   // floor(log2(amax))
+  const int sh = 14 - e;
+  return sh < -126 ? -126 : (sh > 126 ? 126 : sh);
+}
+
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+  float m[16];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) m[i] = fmaxf(v[2 * i], v[2 * i + 1]);
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(v[2 * i], v[2 * i + 1]);
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1)
+  for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
     for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
   return m[0];
@@ -117,26 +154,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
   auto BAR = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
   DeviceStatus* st = a.status;
   const uint64_t limit = cfg.limit_ns;
+  grid_dep_launch();   // the combine kernel may start its weight loads early
 
   // ---- prologue: barriers, validation, ancestor masks, TMEM ------------------------
   if (tid == 0) {
     mbar_init(BAR(B_QR_FULL), 1);
-    mbar_init(BAR(B_Q_READY), 4);
+    mbar_init(BAR(B_Q_READY), 8);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(BAR(B_KV_FULL + i), 1);
       mbar_init(BAR(B_KV_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_P_FULL + i), 4);
+      mbar_init(BAR(B_S_SENT + i), 4);    // sender warps have read the scores
+      mbar_init(BAR(B_P_FULL + i), 8);
+      mbar_init(BAR(B_HMAX + i), 8);
       mbar_init(BAR(B_P_EMPTY + i), 1);
+      mbar_init(BAR(B_RX_FULL + i), 1);   // armed with expect_tx; filled by the peer's st.async
+      mbar_init(BAR(B_TX_OK + i), 8);     // one relaxed arrival per peer softmax warp
     }
     mbar_init(BAR(B_O_FULL), 1);
-    mbar_init(BAR(B_RX_FULL), 1);   // armed with expect_tx; filled by the peer's st.async
-    mbar_init(BAR(B_TX_OK), 4);     // one relaxed arrival per peer softmax warp
     mbar_init(BAR(B_STALL), 1);
     mbar_init(BAR(B_MMA_DONE), 1);
-    mbar_expect_tx(BAR(B_RX_FULL), kRxBytes);   // phase 0 of the score exchange
+    mbar_init(BAR(B_LSUM), 8);
+    mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchange of tiles 0 and 1
+    mbar_expect_tx(BAR(B_RX_FULL + 1), kRxBytes);
     fence_mbar_init();
     int L = 0;
     int ok = prefix_ok(a, b, &L) ? 1 : 0;
@@ -156,10 +198,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     misc[2] = L;
     misc[3] = 1;   // tree ok until a walker says otherwise
   }
+  int32_t* par_s = reinterpret_cast<int32_t*>(sm + OFF_PAR);
+  if (tid < a.N) par_s[tid] = a.parent[(long long)b * a.N + tid];
   __syncthreads();
   if (tid < a.N) {
     uint32_t m[4];
-    bool good = ancestor_mask(a, b, tid, m);
+    bool good = ancestor_mask_smem(a, b, par_s, tid, m);
     anc[4 * tid + 0] = m[0]; anc[4 * tid + 1] = m[1];
     anc[4 * tid + 2] = m[2]; anc[4 * tid + 3] = m[3];
     if (!good) misc[3] = 0;
@@ -193,7 +237,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       }
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
-        const int stg = j & (kStages - 1);
+        const int stg = j % kStages;
         if (j >= kStages &&
             !wait(BAR(B_KV_EMPTY + stg), ((j / kStages) - 1) & 1, st, limit, W_KV_EMPTY))
           break;
@@ -215,7 +259,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       // Drain: every issued copy has landed before this CTA may exit.
       if (rank == 0) wait(BAR(B_QR_FULL), 0, st, limit, W_DRAIN);
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-        wait(BAR(B_KV_FULL + (j & (kStages - 1))), (j / kStages) & 1, st, limit, W_DRAIN);
+        wait(BAR(B_KV_FULL + j % kStages), (j / kStages) & 1, st, limit, W_DRAIN);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -227,8 +271,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       if (alive && rank == 0) alive = wait(BAR(B_QR_FULL), 0, st, limit, W_Q);
       for (int j = 0; alive && j <= nt; ++j) {
         if (j < nt) {
-          const int stg = j & (kStages - 1), buf = j & 1;
+          const int stg = j % kStages, buf = j & 1;
           alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
+          // the score buffer is rewritten: the sender warps must have read tile j-2
+          if (alive && j >= 2)
+            alive = wait(BAR(B_S_SENT + buf), ((j >> 1) - 1) & 1, st, limit, W_S_SENT);
           if (!alive) break;
           tc_fence_after();
           const uint32_t d = tmem + kColSP + 64 * buf;
@@ -249,7 +296,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           mma_commit(BAR(B_S_FULL + buf));
         }
         if (j >= 1) {
-          const int jj = j - 1, stg = jj & (kStages - 1), buf = jj & 1;
+          const int jj = j - 1, stg = jj % kStages, buf = jj & 1;
           alive = wait(BAR(B_P_FULL + buf), (jj >> 1) & 1, st, limit, W_P_FULL);
           if (!alive) break;
           tc_fence_after();
@@ -271,9 +318,57 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
     }
     __syncwarp();
+  } else if (warp < 6) {
+    // ---- sender warps 2..5: own partial scores -> the peer's receive buffer ----------
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+    bool alive = true;
+    for (int j = 0; alive && j < nt; ++j) {
+      const int buf = j & 1;
+      alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
+      if (!alive) break;
+      tc_fence_after();
+      float sv[2][32];
+      tmem_ld32(tmem + lane_addr + kColSP + 64 * buf, sv[0]);
+      tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32, sv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_S_SENT + buf));
+      // the peer has consumed what we sent into this receive buffer two tiles ago
+      if (j >= 2) {
+        alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK + buf), ((j >> 1) - 1) & 1, st, limit,
+                                             W_TX_OK));
+        if (!alive) break;
+      }
+      const uint32_t rx_remote = mapa(sbase + OFF_RX + buf * kRxStride + r * 16, peer);
+      const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL + buf), peer);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(sv[hh][k]));
+        const int sh = fp16_shift(amax);
+        const float sc = pow2f(sh);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            __half2 h = __floats2half2_rn(sv[hh][8 * v + 2 * u] * sc, sv[hh][8 * v + 2 * u + 1] * sc);
+            w[u] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          st_async_v4u(rx_remote + (4 * hh + v) * BM * 16, w[0], w[1], w[2], w[3], rxfull_remote);
+        }
+        st_async_u32(mapa(sbase + OFF_RX + buf * kRxStride + kRxData + (hh * BM + r) * 4, peer),
+                     (uint32_t)sh, rxfull_remote);
+      }
+    }
   } else {
-    // ---- Q load, score exchange, softmax, P, epilogue (warps 2..5) --------------------
+    // ---- softmax warps 6..13: two threads per query row, 32 key columns each --------------
     const int q = warp & 3;                      // TMEM lane quadrant of this warp
+    const int hh = (warp - 6) >> 2;              // which half of the 64 key columns
     const int r = q * 32 + lane;                 // row within the tile = TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
     const int rr = rt * BM + r;                  // row within the request
@@ -284,27 +379,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       an0 = anc[4 * node]; an1 = anc[4 * node + 1]; an2 = anc[4 * node + 2]; an3 = anc[4 * node + 3];
     }
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
-    float m_used = -INFINITY, l_sum = 0.f;
+    float* hmax = reinterpret_cast<float*>(sm + OFF_HMAX);
+    float* lsum = reinterpret_cast<float*>(sm + OFF_LSUM);
+    float m_used = -INFINITY, l_half = 0.f;
     bool alive = true;
-    const uint32_t rx_local = sbase + OFF_RX + r * 16;
-    const uint32_t rx_remote = mapa(rx_local, peer);
-    const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL), peer);
-    const uint32_t txok_remote = mapa(BAR(B_TX_OK), peer);
 
     if (nt > 0) {
-      // q_lat half of this row -> TMEM columns [kColQ, kColQ + 128) as bf16 pairs.
+      grid_dep_wait();   // q_lat is written by the absorb kernel
+      // this thread's 64 bf16 pairs of the q_lat half -> TMEM [kColQ + 64 hh, +64)
       const uint4* src = reinterpret_cast<const uint4*>(
           static_cast<const __nv_bfloat16*>(a.q_lat) + (req_row0 + (row_valid ? rr : 0)) * 512 +
-          rank * kHalf);
+          rank * kHalf + 128 * hh);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           uint4 x = row_valid ? src[8 * c + v] : make_uint4(0u, 0u, 0u, 0u);
           w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
         }
-        tmem_st32u(tmem + lane_addr + kColQ + 32 * c, w);
+        tmem_st32u(tmem + lane_addr + kColQ + 64 * hh + 32 * c, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -315,50 +409,66 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL))
       alive = __all_sync(0xffffffffu, wait(BAR(B_STALL), 0, st, limit, W_STALL));
 
+    int consumed = 0;                            // exchange tiles received so far
     for (int j = 0; alive && j < nt; ++j) {
       const int buf = j & 1;
       alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
       if (!alive) break;
       tc_fence_after();
-      float sv[64];
+      float sv[32];
+      tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32 * hh, sv);
+      tmem_wait_ld();
+
+      // The same fp16 rounding of our own partial that the peer receives, so
+      // both CTAs form the identical sum q(S0) + q(S1) and agree bit for bit.
       {
-        float t0v[32], t1v[32];
-        tmem_ld32(tmem + lane_addr + kColSP + 64 * buf, t0v);
-        tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32, t1v);
-        tmem_wait_ld();
+        float av[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) { sv[k] = t0v[k]; sv[32 + k] = t1v[k]; }
+        for (int k = 0; k < 32; ++k) av[k] = fabsf(sv[k]);
+        const int osh = fp16_shift(max32(av));
+        const float osc = pow2f(osh), oinv = pow2f(-osh);
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float2 f = __half22float2(__floats2half2_rn(sv[k] * osc, sv[k + 1] * osc));
+          sv[k] = f.x * oinv;
+          sv[k + 1] = f.y * oinv;
+        }
       }
 
-      // exchange the partial scores with the peer CTA: asynchronous remote
-      // stores whose bytes complete the peer's RX_FULL phase (no fences)
-      if (j >= 1) {
-        alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK), (j - 1) & 1, st, limit, W_TX_OK));
-        if (!alive) break;
-      }
-#pragma unroll
-      for (int v = 0; v < 16; ++v)
-        st_async_v4(rx_remote + v * BM * 16, sv[4 * v], sv[4 * v + 1], sv[4 * v + 2],
-                    sv[4 * v + 3], rxfull_remote);
-      alive = __all_sync(0xffffffffu, wait<true>(BAR(B_RX_FULL), j & 1, st, limit, W_RX_FULL));
+      // + the peer's partial scores for these columns (its st.async filled rx[buf])
+      alive = __all_sync(0xffffffffu,
+                         wait<true>(BAR(B_RX_FULL + buf), (j >> 1) & 1, st, limit, W_RX_FULL));
       if (!alive) break;
-      if (r == 0 && j + 1 < nt) mbar_expect_tx(BAR(B_RX_FULL), kRxBytes);   // arm next phase
+      consumed = j + 1;
+      if (r == 0 && hh == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
+      {
+        const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
+        int psh;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(psh)
+                     : "r"(rxb + kRxData + (hh * BM + r) * 4) : "memory");
+        const float inv = pow2f(-psh);
 #pragma unroll
-      for (int v = 0; v < 16; ++v) {
-        float x0, x1, x2, x3;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(x0), "=f"(x1), "=f"(x2), "=f"(x3) : "r"(rx_local + v * BM * 16)
-                     : "memory");
-        sv[4 * v] += x0; sv[4 * v + 1] += x1; sv[4 * v + 2] += x2; sv[4 * v + 3] += x3;
+        for (int v = 0; v < 4; ++v) {
+          uint32_t w[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                       : "r"(rxb + ((4 * hh + v) * BM + r) * 16) : "memory");
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[u]));
+            sv[8 * v + 2 * u] += f.x * inv;       // exact scaling, then one rounding
+            sv[8 * v + 2 * u + 1] += f.y * inv;
+          }
+        }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote_relaxed(txok_remote);   // rx values consumed
+      if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));  // consumed
 
-      // visibility mask (only tiles that reach past the prefix), tile max
-      const int t0 = k0 + j * BN;
-      if (!(row_valid && t0 + BN <= L)) {
+      // visibility mask (only tiles that reach past the prefix)
+      const int t0 = k0 + j * BN + 32 * hh;
+      if (!(row_valid && t0 + 32 <= L)) {
 #pragma unroll
-        for (int k = 0; k < BN; ++k) {
+        for (int k = 0; k < 32; ++k) {
           const int t = t0 + k;
           bool vis = false;
           if (row_valid && t < k1) {
@@ -373,28 +483,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           if (!vis) sv[k] = -INFINITY;
         }
       }
-      const float m_tile = max64(sv) * sl2;
+      // tile max of the full row: the two half-row threads meet (bounded wait)
+      hmax[(buf * 2 + hh) * BM + r] = max32(sv);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_HMAX + buf));
+      alive = __all_sync(0xffffffffu, wait(BAR(B_HMAX + buf), (j >> 1) & 1, st, limit, W_S_FULL));
+      if (!alive) break;
+      const float m_tile =
+          fmaxf(hmax[(buf * 2) * BM + r], hmax[(buf * 2 + 1) * BM + r]) * sl2;
 
-      // lazy rescale: move the reference max only when it grows by > 8 (log2)
+      // lazy rescale: move the reference max only when it grows by > 8 (log2);
+      // both half-row threads take the same decision from the same inputs
       float alpha = 1.f;
       bool rescale = false;
       if (m_tile > m_used + 8.f) {
         if (m_used != -INFINITY) { alpha = ex2(m_used - m_tile); rescale = true; }
-        l_sum *= alpha;
+        l_half *= alpha;
         m_used = m_tile;
       }
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-      uint32_t packed[32];
-      float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t packed[16];
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < BN; k += 2) {
+      for (int k = 0; k < 32; k += 2) {
         const float p0 = ex2(fmaf(sv[k], sl2, neg_m));
         const float p1 = ex2(fmaf(sv[k + 1], sl2, neg_m));
         const uint32_t h2 = pack_bf16x2(p0, p1);
         packed[k >> 1] = h2;
-        ps[(k >> 1) & 7] += __uint_as_float(h2 << 16) + __uint_as_float(h2 & 0xffff0000u);
+        ps[(k >> 1) & 3] += __uint_as_float(h2 << 16) + __uint_as_float(h2 & 0xffff0000u);
       }
-      l_sum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l_half += (ps[0] + ps[1]) + (ps[2] + ps[3]);
 
       // the P buffer is free once P.V of tile j-2 (same buffer) has completed;
       // O is stable once P.V of tile j-1 has completed
@@ -410,29 +528,46 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           if (!alive) break;
         }
         tc_fence_after();
-        for (int c = 0; c < kHalf / 32; ++c) {
+        for (int c = 0; c < kHalf / 64; ++c) {        // this thread's 128 of the 256 O columns
           float ov[32];
-          tmem_ld32(tmem + lane_addr + kColO + 32 * c, ov);
+          const uint32_t oa = tmem + lane_addr + kColO + 128 * hh + 32 * c;
+          tmem_ld32(oa, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) ov[k] *= alpha;
-          tmem_st32(tmem + lane_addr + kColO + 32 * c, ov);
+          tmem_st32(oa, ov);
         }
       }
+      // P overwrites the scores: the sender warps must have read this tile
+      alive = __all_sync(0xffffffffu, wait(BAR(B_S_SENT + buf), (j >> 1) & 1, st, limit, W_S_SENT));
+      if (!alive) break;
       tc_fence_after();
-      tmem_st32u(tmem + lane_addr + kColSP + 64 * buf, packed);
+      tmem_st16u(tmem + lane_addr + kColSP + 64 * buf + 16 * hh, packed);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_P_FULL + buf));
     }
 
+    // After an abort, let score rows the peer may still be sending land before exit
+    // (receive phases that were armed but not consumed); bounded, errors ignored.
+    for (int t = consumed; t < consumed + 2 && t < nt; ++t)
+      drain_wait(BAR(B_RX_FULL + (t & 1)), (t >> 1) & 1, 200000ull);
+
     // ---- epilogue: unnormalised partial o_lat half, (m, l) -----------------------------
     if (alive && nt > 0)
       alive = __all_sync(0xffffffffu, wait(BAR(B_O_FULL), 0, st, limit, W_O_FULL));
+    float l_sum = 0.f;
+    if (alive && nt > 0) {
+      lsum[hh * BM + r] = l_half;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_LSUM));
+      alive = __all_sync(0xffffffffu, wait(BAR(B_LSUM), 0, st, limit, W_O_FULL));
+      if (alive) l_sum = lsum[r] + lsum[BM + r];
+    }
     // tcgen05.ld is warp-collective: every lane loads, only valid rows store.
     const bool has_data = ok && alive && nt > 0 && row_valid && l_sum > 0.f;
-    if (ok && alive && row_valid) {
+    if (ok && alive && row_valid && hh == 0) {
       const long long rows = (long long)a.B * a.N * a.H;
       float* ml = a.part_ml + ((long long)s * rows + req_row0 + rr) * 2;
       if (rank == 0) {
@@ -443,11 +578,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     if (ok && alive && nt > 0 && __any_sync(0xffffffffu, has_data)) {
       const long long rows = (long long)a.B * a.N * a.H;
       float* po = a.part_o + ((long long)s * rows + req_row0 + (has_data ? rr : 0)) * a.d_c +
-                  rank * kHalf;
+                  rank * kHalf + 128 * hh;
       tc_fence_after();
-      for (int c = 0; c < kHalf / 32; ++c) {
+      for (int c = 0; c < 4; ++c) {
         float ov[32];
-        tmem_ld32(tmem + lane_addr + kColO + 32 * c, ov);
+        tmem_ld32(tmem + lane_addr + kColO + 128 * hh + 32 * c, ov);
         tmem_wait_ld();
         if (has_data) {
 #pragma unroll
@@ -568,8 +703,9 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
   e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<(unsigned)(2 * items), kThreads, kSmemBytes, st>>>(tqr, tck, tkr, a, cfg);
-  e = cudaGetLastError();
+  // Overlap with the absorb kernel's tail unless phase events split the call.
+  e = launch_ex(attn_tc_kernel, dim3((unsigned)(2 * items)), dim3(kThreads), kSmemBytes, st,
+                /*pdl=*/ev == nullptr && !simt_proj, tqr, tck, tkr, a, cfg);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], st);
   return simt_proj ? launch_combine_uproj(a, p, st, ev) : launch_combine_uproj_tc(a, p, st, ev);

@@ -56,6 +56,7 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int off_b = ab_off_b(a.d_nope), off_bar = ab_off_bar(a.d_nope);
   const uint32_t bar_full = sbase + off_bar, bar_mma = bar_full + 8;
   volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + off_bar + 16);
+  grid_dep_launch();   // the attention kernel may start its prologue early
 
   if (tid == 0) {
     mbar_init(bar_full, 1);
@@ -156,6 +157,8 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
     for (int k = 0; k < 8; ++k)
       tma_load_2d(sbase + k * 128 * 128, &tm_w, bar_full, 64 * k, h * 128);
   }
+
+  grid_dep_wait();   // the split partials are written by the attention kernel
 
   // Split weights per row, with 1 / sum_s e^{m_s - m*} l_s folded in.
   if (tid < UP_NR) {
@@ -311,9 +314,11 @@ cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t s
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[3], st);   // the combine is fused into the up-projection
   const unsigned nblk = (unsigned)(((long long)a.B * a.N + UP_NR - 1) / UP_NR);
-  combine_uproj_tc_kernel<<<dim3(a.H, nblk), UP_THREADS, UP_SMEM, st>>>(tw, a);
+  // Overlap with the attention kernel's tail unless phase events split the call.
+  e = launch_ex(combine_uproj_tc_kernel, dim3(a.H, nblk), dim3(UP_THREADS), UP_SMEM, st,
+                /*pdl=*/ev == nullptr, tw, a);
   if (ev) cudaEventRecord(ev[4], st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace kdtv
