@@ -35,6 +35,24 @@ UNIT = "us/call"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM bytes (read + write) of one attention-kernel launch, from an ncu
+# capture of that workload (profiles/attn_tc_kernel_<workload>.md), keyed by
+# the SHA-256 of the kernel source the capture was taken on: a changed kernel
+# reports null until it is captured again.
+ATTN_TRAFFIC = {}
+
+
+def attn_traffic(workload):
+    rec = ATTN_TRAFFIC.get(workload)
+    if rec is None:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "speculative_decoding_tree_mla_gb300", "csrc", "kdtv_tc.cu")
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    return rec[1] if digest == rec[0] else None
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -382,7 +400,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": wl.spec.dtype,
             "data": "synthetic", "config": config_dict(wl),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tc,
-                         "unit": "TFLOP/s", "frac": tflops / peak_tc, "traffic": None,
+                         "unit": "TFLOP/s", "frac": tflops / peak_tc,
+                         "traffic": attn_traffic(args.config),
                          "kernel": "attention (tree-masked scores, online softmax, P.c_kv)",
                          "peak_source": f"{pk_kind} bf16_tflops (burst)"},
             "call_roofline": {"t_roof_us": roof_us, "frac": roof_us / us_call,

@@ -58,7 +58,8 @@ int make_plan(const kdtv_dims* d, Plan* p) {
   p->tensor_core = use_tensor_cores(d);
   p->rows = d->B * d->N * d->H;
   p->t_cap = d->page_size ? d->max_pages * d->page_size : d->t_stride;
-  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const int sms = sm_count() > 0 ? sm_count() : 152;   // no device: size for a GB300
+  p->sms = sms;
   int chunk;
   if (p->tensor_core) {
     chunk = tc_chunk(d, sms);

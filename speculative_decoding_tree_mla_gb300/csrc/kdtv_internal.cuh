@@ -41,6 +41,7 @@ struct Plan {
   int chunk;              // keys per split
   int splits;             // splits per request (ceil(t_cap / chunk))
   int heads_per_cta;      // SIMT attention: heads sharing one CTA
+  int sms;                // streaming multiprocessors of the current device
   size_t off_qlat, off_part_o, off_part_ml, off_olat, total;
 };
 

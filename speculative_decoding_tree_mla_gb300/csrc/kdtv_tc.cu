@@ -52,7 +52,8 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 64;           // keys per tile (MMA N of Q.K^T)
 constexpr int CH = 64;           // bf16 columns per 128-byte swizzled chunk
 constexpr int kHalf = 256;       // latent columns per CTA
-constexpr int kStages = 4;
+constexpr int kStages = 3;
+constexpr int kPrefetch = 3;     // key tiles prefetched into L2 beyond the stages in flight
 constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk per key tile
 constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
 constexpr int kQRopeBytes = BM * CH * 2;
@@ -64,7 +65,9 @@ constexpr int kQRopeBytes = BM * CH * 2;
 // contiguous 512-byte block; the exponents follow as [2][BM] words.
 constexpr int kRxData = BM * BN * 2;
 constexpr int kRxBytes = kRxData + 2 * BM * 4;
-constexpr int kThreads = 448;    // TMA, MMA, 4 sender warps, 8 softmax warps (2 per row)
+constexpr int kThreads = 480;    // TMA, QK^T issuer, 4 senders, 8 softmax (2 per row), P.V issuer
+constexpr int kWarpPV = 14;      // the P.V issuer warp
+constexpr int kPBytes = BM * BN * 2;   // one P tile: 128 rows x 64 keys bf16, 128B-swizzled
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;
 constexpr int kColQ = 256;
@@ -73,38 +76,45 @@ constexpr int kColSP = 384;      // + 64 * buffer
 constexpr int OFF_KV = 0;
 constexpr int OFF_QR = OFF_KV + kStages * kMaxCh * kKVChunk;
 constexpr int kRxStride = (kRxBytes + 1023) / 1024 * 1024;
-constexpr int OFF_RX = OFF_QR + kQRopeBytes;                 // two receive buffers
+constexpr int OFF_P = OFF_QR + kQRopeBytes;                  // two P tiles (A of P.V)
+constexpr int OFF_RX = OFF_P + 2 * kPBytes;                   // two receive buffers
 constexpr int OFF_ANC = OFF_RX + 2 * kRxStride;
 constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 16;               // staged parent[]
 constexpr int OFF_HMAX = OFF_PAR + kMaxNodes * 4;               // [2 tiles][2 halves][BM] floats
 constexpr int OFF_LSUM = OFF_HMAX + 2 * 2 * BM * 4;             // [2 halves][BM] floats
-constexpr int OFF_BAR = OFF_LSUM + 2 * BM * 4;
-constexpr int kNumBars = 32;
+constexpr int OFF_OSH = OFF_LSUM + 2 * BM * 4;             // [2 tiles][2 halves][BM] own fp16 shifts
+constexpr int OFF_BAR = OFF_OSH + 2 * 2 * BM * 4;
+constexpr int kNumBars = 40;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+static_assert(OFF_P % 1024 == 0 && OFF_RX % 1024 == 0 && OFF_QR % 1024 == 0,
+              "128B-swizzled tiles need 1 KiB alignment");
+static_assert(kThreads == 32 * (kWarpPV + 1), "warp roles");
 
 // Barrier indices (derived from kStages so the groups never overlap).
 enum Bar : int {
   B_QR_FULL = 0, B_Q_READY = 1, B_KV_FULL = 2,
   B_KV_EMPTY = B_KV_FULL + kStages,
   B_S_FULL = B_KV_EMPTY + kStages,   // [2]
-  B_S_SENT = B_S_FULL + 2,           // [2]
-  B_P_FULL = B_S_SENT + 2,           // [2]
+  B_S_FREE = B_S_FULL + 2,           // [2] the softmax has read the quantised own scores
+  B_OWN = B_S_FREE + 2,              // [2] senders wrote the quantised own scores
+  B_P_FULL = B_OWN + 2,              // [2]
   B_P_EMPTY = B_P_FULL + 2,          // [2]
   B_O_FULL = B_P_EMPTY + 2,
   B_RX_FULL = B_O_FULL + 1,          // [2]
   B_TX_OK = B_RX_FULL + 2,           // [2]
   B_STALL = B_TX_OK + 2,
   B_MMA_DONE = B_STALL + 1,
-  B_HMAX = B_MMA_DONE + 1,           // [2] the two half-row threads met (tile max)
-  B_LSUM = B_HMAX + 2,               // the two half-row threads met (row sums)
+  B_HMAX = B_MMA_DONE + 1,           // [2][4] the two half-row warps of a quadrant met (tile max)
+  B_LSUM = B_HMAX + 8,               // the two half-row threads met (row sums)
   B_COUNT = B_LSUM + 1
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 
 // Wait sites (reported as the timeout detail).
 enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK, W_RX_FULL,
-            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_SENT };
+            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_HMAX, W_OWN };
 
 struct TcCfg {
   int row_tiles;               // ceil(N * H / 128)
@@ -115,11 +125,13 @@ struct TcCfg {
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
 // Shift that maps max |v| into [2^14, 2^15): the fp16 range with headroom.
+// Capped at 100 so that every nonzero fp16 value times 2^-shift is a normal
+// float: the dequantised products are then exact in both CTAs.
 __device__ __forceinline__ int fp16_shift(float amax) {
   if (!(amax > 0.f)) return 0;
   const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;   // floor(log2(amax))
   const int sh = 14 - e;
-  return sh < -126 ? -126 : (sh > 126 ? 126 : sh);
+  return sh < -126 ? -126 : (sh > 100 ? 100 : sh);
 }
 
 __device__ __forceinline__ float max32(const float (&v)[32]) {
@@ -166,16 +178,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_S_SENT + i), 4);    // sender warps have read the scores
+      mbar_init(BAR(B_S_FREE + i), 8);    // 8 softmax warps have read the own scores
+      mbar_init(BAR(B_OWN + i), 4);       // 4 sender warps quantised them
       mbar_init(BAR(B_P_FULL + i), 8);
-      mbar_init(BAR(B_HMAX + i), 8);
       mbar_init(BAR(B_P_EMPTY + i), 1);
       mbar_init(BAR(B_RX_FULL + i), 1);   // armed with expect_tx; filled by the peer's st.async
       mbar_init(BAR(B_TX_OK + i), 8);     // one relaxed arrival per peer softmax warp
     }
     mbar_init(BAR(B_O_FULL), 1);
     mbar_init(BAR(B_STALL), 1);
-    mbar_init(BAR(B_MMA_DONE), 1);
+    mbar_init(BAR(B_MMA_DONE), 2);      // both MMA issuers drained
+    for (int i = 0; i < 8; ++i) mbar_init(BAR(B_HMAX + i), 2);
     mbar_init(BAR(B_LSUM), 8);
     mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchange of tiles 0 and 1
     mbar_expect_tx(BAR(B_RX_FULL + 1), kRxBytes);
@@ -235,19 +248,27 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         mbar_expect_tx(BAR(B_QR_FULL), kQRopeBytes);
         tma_load_2d(sbase + OFF_QR, &tm_qrope, BAR(B_QR_FULL), 0, qrow);
       }
+      // Cache row of key tile j (paged: through the page table).
+      auto tile_row = [&](int j) -> int {
+        const int t0 = k0 + j * BN;
+        return a.page_size ? a.page_table[(long long)b * a.max_pages + t0 / a.page_size] * a.page_size
+                           : b * a.t_stride + t0;
+      };
+      // L2 prefetch kPrefetch tiles ahead of the loads, so that a refilled
+      // stage finds its tile in L2 rather than in DRAM.
+      auto prefetch = [&](int j) {
+        const int row = tile_row(j);
+        for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_ckv, (int)rank * kHalf + c * CH, row);
+        if (rank == 0) tma_prefetch_2d(&tm_krope, 0, row);
+      };
+      for (int j = kStages; j < kStages + kPrefetch && j < nt; ++j) prefetch(j);
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int stg = j % kStages;
         if (j >= kStages &&
             !wait(BAR(B_KV_EMPTY + stg), ((j / kStages) - 1) & 1, st, limit, W_KV_EMPTY))
           break;
-        const int t0 = k0 + j * BN;
-        int row;
-        if (a.page_size) {
-          row = a.page_table[(long long)b * a.max_pages + t0 / a.page_size] * a.page_size;
-        } else {
-          row = b * a.t_stride + t0;
-        }
+        const int row = tile_row(j);
         mbar_expect_tx(BAR(B_KV_FULL + stg), nch * kKVChunk);
         const uint32_t dst = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
         for (int c = 0; c < 4; ++c)
@@ -255,6 +276,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                       (int)rank * kHalf + c * CH, row);
         if (rank == 0) tma_load_2d(dst + 4 * kKVChunk, &tm_krope, BAR(B_KV_FULL + stg), 0, row);
         issued = j + 1;
+        if (j + kStages + kPrefetch < nt) prefetch(j + kStages + kPrefetch);
       }
       // Drain: every issued copy has landed before this CTA may exit.
       if (rank == 0) wait(BAR(B_QR_FULL), 0, st, limit, W_DRAIN);
@@ -263,63 +285,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---- MMA issuer ----------------------------------------------------------------
+    // ---- Q.K^T issuer (also owns TMEM) ------------------------------------------------
     if (lane == 0 && nt > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
       bool alive = wait(BAR(B_Q_READY), 0, st, limit, W_Q);
       if (alive && rank == 0) alive = wait(BAR(B_QR_FULL), 0, st, limit, W_Q);
-      for (int j = 0; alive && j <= nt; ++j) {
-        if (j < nt) {
-          const int stg = j % kStages, buf = j & 1;
-          alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
-          // the score buffer is rewritten: the sender warps must have read tile j-2
-          if (alive && j >= 2)
-            alive = wait(BAR(B_S_SENT + buf), ((j >> 1) - 1) & 1, st, limit, W_S_SENT);
-          if (!alive) break;
-          tc_fence_after();
-          const uint32_t d = tmem + kColSP + 64 * buf;
-          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+      for (int j = 0; alive && j < nt; ++j) {
+        const int stg = j % kStages, buf = j & 1;
+        alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
+        // the score buffer is rewritten: senders and softmax must have read tile j-2
+        if (alive && j >= 2)
+          alive = wait(BAR(B_S_FREE + buf), ((j >> 1) - 1) & 1, st, limit, W_S_FREE);
+        if (!alive) break;
+        tc_fence_after();
+        const uint32_t d = tmem + kColSP + 64 * buf;
+        const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
 #pragma unroll
-          for (int kk = 0; kk < kHalf / 16; ++kk) {     // latent half: A = q_lat in TMEM
-            uint64_t bd = smem_desc(kv + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
-            mma_bf16_ts(d, tmem + kColQ + 8 * kk, bd, kIdescQK, kk > 0);
-          }
-          if (rank == 0) {
-#pragma unroll
-            for (int kk = 0; kk < CH / 16; ++kk) {      // rope: A = q_rope in smem
-              uint64_t ad = smem_desc(sbase + OFF_QR + kk * 32, 16, 1024);
-              uint64_t bd = smem_desc(kv + 4 * kKVChunk + kk * 32, 16, 1024);
-              mma_bf16(d, ad, bd, kIdescQK, 1);
-            }
-          }
-          mma_commit(BAR(B_S_FULL + buf));
+        for (int kk = 0; kk < kHalf / 16; ++kk) {       // latent half: A = q_lat in TMEM
+          uint64_t bd = smem_desc(kv + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
+          mma_bf16_ts(d, tmem + kColQ + 8 * kk, bd, kIdescQK, kk > 0);
         }
-        if (j >= 1) {
-          const int jj = j - 1, stg = jj % kStages, buf = jj & 1;
-          alive = wait(BAR(B_P_FULL + buf), (jj >> 1) & 1, st, limit, W_P_FULL);
-          if (!alive) break;
-          tc_fence_after();
-          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+        if (rank == 0) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            // V = c_kv columns of this CTA, MN-major: 64-column chunks are
-            // kKVChunk apart (LBO), 8-key groups 1024 B apart (SBO).
-            uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
-            mma_bf16_ts(tmem + kColO, tmem + kColSP + 64 * buf + 8 * kk, bd, kIdescPV,
-                        (jj > 0 || kk > 0));
+          for (int kk = 0; kk < CH / 16; ++kk) {        // rope: A = q_rope in smem
+            uint64_t ad = smem_desc(sbase + OFF_QR + kk * 32, 16, 1024);
+            uint64_t bd = smem_desc(kv + 4 * kKVChunk + kk * 32, 16, 1024);
+            mma_bf16(d, ad, bd, kIdescQK, 1);
           }
-          mma_commit(BAR(B_KV_EMPTY + stg));
-          mma_commit(BAR(B_P_EMPTY + buf));
         }
+        mma_commit(BAR(B_S_FULL + buf));
       }
-      if (alive) mma_commit(BAR(B_O_FULL));
-      mma_commit(BAR(B_MMA_DONE));               // drain every issued MMA
+      mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
       wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
     }
     __syncwarp();
   } else if (warp < 6) {
     // ---- sender warps 2..5: own partial scores -> the peer's receive buffer ----------
+    int* osh = reinterpret_cast<int*>(sm + OFF_OSH);
     const int q = warp & 3;
     const int r = q * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
@@ -333,9 +335,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       tmem_ld32(tmem + lane_addr + kColSP + 64 * buf, sv[0]);
       tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32, sv[1]);
       tmem_wait_ld();
+      // Quantise the partial scores once, to fp16 with an exact power-of-two
+      // scale per 32-column half; the same words go to the peer and, through
+      // the first 32 columns of this score buffer, to our own softmax warps.
+      uint32_t w[32];
+      int sh[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(sv[hh][k]));
+        sh[hh] = fp16_shift(amax);
+        const float sc = pow2f(sh[hh]);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          __half2 h2 = __floats2half2_rn(sv[hh][2 * k] * sc, sv[hh][2 * k + 1] * sc);
+          w[16 * hh + k] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+      }
+      tmem_st32u(tmem + lane_addr + kColSP + 64 * buf, w);
+      osh[(buf * 2 + 0) * BM + r] = sh[0];
+      osh[(buf * 2 + 1) * BM + r] = sh[1];
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_S_SENT + buf));
+      if (lane == 0) mbar_arrive(BAR(B_OWN + buf));
       // the peer has consumed what we sent into this receive buffer two tiles ago
       if (j >= 2) {
         alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK + buf), ((j >> 1) - 1) & 1, st, limit,
@@ -345,27 +369,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       const uint32_t rx_remote = mapa(sbase + OFF_RX + buf * kRxStride + r * 16, peer);
       const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL + buf), peer);
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float amax = 0.f;
+      for (int v = 0; v < 8; ++v)
+        st_async_v4u(rx_remote + v * BM * 16, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3],
+                     rxfull_remote);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(sv[hh][k]));
-        const int sh = fp16_shift(amax);
-        const float sc = pow2f(sh);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            __half2 h = __floats2half2_rn(sv[hh][8 * v + 2 * u] * sc, sv[hh][8 * v + 2 * u + 1] * sc);
-            w[u] = *reinterpret_cast<uint32_t*>(&h);
-          }
-          st_async_v4u(rx_remote + (4 * hh + v) * BM * 16, w[0], w[1], w[2], w[3], rxfull_remote);
-        }
+      for (int hh = 0; hh < 2; ++hh)
         st_async_u32(mapa(sbase + OFF_RX + buf * kRxStride + kRxData + (hh * BM + r) * 4, peer),
-                     (uint32_t)sh, rxfull_remote);
-      }
+                     (uint32_t)sh[hh], rxfull_remote);
     }
-  } else {
+  } else if (warp < kWarpPV) {
     // ---- softmax warps 6..13: two threads per query row, 32 key columns each --------------
     const int q = warp & 3;                      // TMEM lane quadrant of this warp
     const int hh = (warp - 6) >> 2;              // which half of the 64 key columns
@@ -381,6 +393,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
     float* hmax = reinterpret_cast<float*>(sm + OFF_HMAX);
     float* lsum = reinterpret_cast<float*>(sm + OFF_LSUM);
+    const int* osh = reinterpret_cast<const int*>(sm + OFF_OSH);
     float m_used = -INFINITY, l_half = 0.f;
     bool alive = true;
 
@@ -412,41 +425,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     int consumed = 0;                            // exchange tiles received so far
     for (int j = 0; alive && j < nt; ++j) {
       const int buf = j & 1;
-      alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
+      alive = __all_sync(0xffffffffu, wait(BAR(B_OWN + buf), (j >> 1) & 1, st, limit, W_OWN));
       if (!alive) break;
       tc_fence_after();
-      float sv[32];
-      tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32 * hh, sv);
+      // own partial scores of this half: 16 fp16 pairs written by the sender warps
+      uint32_t ow[16];
+      tmem_ld16u(tmem + lane_addr + kColSP + 64 * buf + 16 * hh, ow);
+      const int own_sh = osh[(buf * 2 + hh) * BM + r];
       tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));   // QK^T of tile j+2 may overwrite
 
-      // The same fp16 rounding of our own partial that the peer receives, so
-      // both CTAs form the identical sum q(S0) + q(S1) and agree bit for bit.
-      {
-        float av[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) av[k] = fabsf(sv[k]);
-        const int osh = fp16_shift(max32(av));
-        const float osc = pow2f(osh), oinv = pow2f(-osh);
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float2 f = __half22float2(__floats2half2_rn(sv[k] * osc, sv[k + 1] * osc));
-          sv[k] = f.x * oinv;
-          sv[k + 1] = f.y * oinv;
-        }
-      }
-
-      // + the peer's partial scores for these columns (its st.async filled rx[buf])
+      // + the peer's partial scores for these columns (its st.async filled rx[buf]).
+      // Both products are exact (fp16 times a power of two), so own + peer
+      // rounds to the same float in both CTAs whichever is added first.
       alive = __all_sync(0xffffffffu,
                          wait<true>(BAR(B_RX_FULL + buf), (j >> 1) & 1, st, limit, W_RX_FULL));
       if (!alive) break;
       consumed = j + 1;
       if (r == 0 && hh == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
+      float sv[32];
       {
         const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
         int psh;
         asm volatile("ld.shared.b32 %0, [%1];" : "=r"(psh)
                      : "r"(rxb + kRxData + (hh * BM + r) * 4) : "memory");
-        const float inv = pow2f(-psh);
+        const float pinv = pow2f(-psh), oinv = pow2f(-own_sh);
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint32_t w[4];
@@ -455,9 +460,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                        : "r"(rxb + ((4 * hh + v) * BM + r) * 16) : "memory");
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[u]));
-            sv[8 * v + 2 * u] += f.x * inv;       // exact scaling, then one rounding
-            sv[8 * v + 2 * u + 1] += f.y * inv;
+            const float2 fp = __half22float2(*reinterpret_cast<__half2*>(&w[u]));
+            const float2 fo = __half22float2(*reinterpret_cast<__half2*>(&ow[4 * v + u]));
+            sv[8 * v + 2 * u] = fmaf(fp.x, pinv, fo.x * oinv);
+            sv[8 * v + 2 * u + 1] = fmaf(fp.y, pinv, fo.y * oinv);
           }
         }
       }
@@ -486,8 +492,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       // tile max of the full row: the two half-row threads meet (bounded wait)
       hmax[(buf * 2 + hh) * BM + r] = max32(sv);
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_HMAX + buf));
-      alive = __all_sync(0xffffffffu, wait(BAR(B_HMAX + buf), (j >> 1) & 1, st, limit, W_S_FULL));
+      if (lane == 0) mbar_arrive(BAR(B_HMAX + 4 * buf + q));
+      alive = __all_sync(0xffffffffu,
+                         wait(BAR(B_HMAX + 4 * buf + q), (j >> 1) & 1, st, limit, W_HMAX));
       if (!alive) break;
       const float m_tile =
           fmaxf(hmax[(buf * 2) * BM + r], hmax[(buf * 2 + 1) * BM + r]) * sl2;
@@ -537,14 +544,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           for (int k = 0; k < 32; ++k) ov[k] *= alpha;
           tmem_st32(oa, ov);
         }
+        tmem_wait_st();
+        tc_fence_before();
       }
-      // P overwrites the scores: the sender warps must have read this tile
-      alive = __all_sync(0xffffffffu, wait(BAR(B_S_SENT + buf), (j >> 1) & 1, st, limit, W_S_SENT));
-      if (!alive) break;
-      tc_fence_after();
-      tmem_st16u(tmem + lane_addr + kColSP + 64 * buf + 16 * hh, packed);
-      tmem_wait_st();
-      tc_fence_before();
+      // P row r, keys 32hh..32hh+31 = 16-byte chunks 4hh..4hh+3 of the row's 128
+      // bytes, stored 128B-swizzled (chunk c of row r at c ^ (r & 7)): the
+      // K-major A operand layout of P.V.
+      {
+        const uint32_t prow = sbase + OFF_P + buf * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t dst = prow + (((4 * hh + v) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(dst), "r"(packed[4 * v]), "r"(packed[4 * v + 1]),
+                          "r"(packed[4 * v + 2]), "r"(packed[4 * v + 3]) : "memory");
+        }
+      }
+      fence_async_smem();                         // visible to the tensor core
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_P_FULL + buf));
     }
@@ -592,6 +608,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         }
       }
     }
+  } else {
+    // ---- P.V issuer (warp 14): O_c += P . c_kv[:, 256c : 256c+256] -------------------
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
+      bool alive = true;
+      for (int j = 0; j < nt; ++j) {
+        const int stg = j % kStages, buf = j & 1;
+        alive = wait(BAR(B_P_FULL + buf), (j >> 1) & 1, st, limit, W_P_FULL);
+        // already complete (Q.K^T of tile j read this stage); orders the TMA data
+        if (alive) alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
+        if (!alive) break;
+        tc_fence_after();
+        const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+        const uint32_t pb = sbase + OFF_P + buf * kPBytes;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // A = P (K-major, 128B rows); B = V = c_kv columns of this CTA,
+          // MN-major: 64-column chunks kKVChunk apart (LBO), 8-key groups 1 KiB apart (SBO).
+          uint64_t ad = smem_desc(pb + kk * 32, 16, 1024);
+          uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
+          mma_bf16(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0));
+        }
+        mma_commit(BAR(B_KV_EMPTY + stg));
+        mma_commit(BAR(B_P_EMPTY + buf));
+      }
+      if (alive) mma_commit(BAR(B_O_FULL));
+      mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
+      wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
+    }
+    __syncwarp();
   }
 
   // ---- teardown ------------------------------------------------------------------------

@@ -51,7 +51,6 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int r0 = blockIdx.z * AB_NR;
   const int BNr = a.B * a.N;
   const int nr = min(AB_NR, BNr - r0);
-  const int n_mma = (nr + 15) & ~15;
   const int kch = a.d_nope / 64;             // 64-wide K chunks
   const int off_b = ab_off_b(a.d_nope), off_bar = ab_off_bar(a.d_nope);
   const uint32_t bar_full = sbase + off_bar, bar_mma = bar_full + 8;
@@ -71,8 +70,8 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 
   bool ok = true;
   if (tid == 0) {
-    const uint32_t a_bytes = 2u * a.d_nope * 128u;
-    mbar_expect_tx(bar_full, a_bytes + kch * AB_NR * 128u);
+    const uint32_t w_bytes = 2u * a.d_nope * 128u;
+    mbar_expect_tx(bar_full, w_bytes + kch * AB_NR * 128u);
     for (int c = 0; c < 2; ++c)       // W_UK[h][:, d0 + 64c : +64]: e-rows x 64 d
       tma_load_2d(sbase + c * a.d_nope * 128, &tm_w, bar_full, d0 + 64 * c, h * a.d_nope);
     for (int k = 0; k < kch; ++k)     // q_nope rows r0.. of head h, e in [64k, 64k+64)
@@ -80,11 +79,13 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
     ok = wait(bar_full, 0, a.status, kLimitNs, 101);
     if (ok) {
       tc_fence_after();
-      const uint32_t idesc = idesc_bf16(AB_M, n_mma, /*a_mn=*/1, /*b_mn=*/0);
+      // D[128 rows x 128 d] = q_nope rows (A, K-major) x W_UK block (B, MN-major);
+      // rows past the last query row are zero-filled by TMA and never stored.
+      const uint32_t idesc = idesc_bf16(AB_NR, AB_M, /*a_mn=*/0, /*b_mn=*/1);
       for (int kk = 0; kk < a.d_nope / 16; ++kk) {
-        // A (MN-major): 64-column atoms a.d_nope*128 B apart, 8 e-rows per 1 KiB.
-        uint64_t ad = smem_desc(sbase + kk * 16 * 128, a.d_nope * 128, 1024);
-        uint64_t bd = smem_desc(sbase + off_b + (kk >> 2) * AB_NR * 128 + (kk & 3) * 32, 16, 1024);
+        uint64_t ad = smem_desc(sbase + off_b + (kk >> 2) * AB_NR * 128 + (kk & 3) * 32, 16, 1024);
+        // B (MN-major): 64-column atoms a.d_nope*128 B apart, 8 e-rows per 1 KiB.
+        uint64_t bd = smem_desc(sbase + kk * 16 * 128, a.d_nope * 128, 1024);
         mma_bf16(tmem, ad, bd, idesc, kk > 0);
       }
     }
@@ -94,18 +95,25 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   ok = wait(bar_mma, 0, a.status, kLimitNs, 102) && ok;
   ok = __all_sync(0xffffffffu, ok);
   tc_fence_after();
-  if (ok) {
-    __nv_bfloat16* ql = static_cast<__nv_bfloat16*>(a.q_lat);
-    const int d = d0 + warp * 32 + lane;
+  if (ok && warp * 32 < nr) {
+    // TMEM lane = query row: each thread writes its row's 128 latent columns
+    // as sixteen 16-byte vectors.
+    const int r = warp * 32 + lane;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.q_lat) +
+                                          ((long long)(r0 + (r < nr ? r : 0)) * a.H + h) * 512 + d0);
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    for (int c0 = 0; c0 < n_mma; c0 += 32) {
-      float v[32];
-      tmem_ld32(tmem + lane_addr + c0, v);
-      tmem_wait_ld();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int r = c0 + j;
-        if (r < nr) ql[((long long)(r0 + r) * a.H + h) * 512 + d] = __float2bfloat16_rn(v[j]);
+    for (int c = 0; c < AB_M / 32; ++c) {
+      float v[32];
+      tmem_ld32(tmem + lane_addr + 32 * c, v);
+      tmem_wait_ld();
+      if (r < nr) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[4 * c + q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
+                                      pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                      pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                                      pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
     }
   }
@@ -115,18 +123,25 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 }
 
 // ---- A5 + A6: split combine fused with the W_UV up-projection -------------------------
-constexpr int UP_NR = 64;                          // query rows (b, i) per CTA
+// UP_NR query rows (b, i) per CTA: 16, 32 or 64, chosen per call so that the
+// grid (heads x row blocks) fills the GPU.  Shared memory: A = W_UV[h] as 8
+// chunks of 128 v-rows x 64 d; B = merged o_lat rows (bf16) as 8 chunks of
+// UP_NR rows x 64 d; per-row split weights; barriers.
 constexpr int UP_MAX_SPLITS = 64;
-constexpr int UP_OFF_B = 8 * 128 * 128;            // A: W_UV[h] as 8 chunks of 128 v x 64 d
-constexpr int UP_OFF_W = UP_OFF_B + 8 * UP_NR * 128;
-constexpr int UP_OFF_BAR = UP_OFF_W + UP_NR * UP_MAX_SPLITS * 4;
-constexpr int UP_SMEM = UP_OFF_BAR + 64 + 1024;
+constexpr int UP_OFF_B = 8 * 128 * 128;
+__host__ __device__ constexpr int up_off_w(int nr) { return UP_OFF_B + 8 * nr * 128; }
+__host__ __device__ constexpr int up_off_bar(int nr) { return up_off_w(nr) + nr * UP_MAX_SPLITS * 4; }
+__host__ __device__ constexpr int up_smem(int nr) { return up_off_bar(nr) + 64 + 1024; }
+__host__ __device__ constexpr int up_tmem_cols(int nr) { return nr < 32 ? 32 : nr; }
 
 constexpr int UP_THREADS = 256;   // all warps merge partials; warps 0-3 read TMEM
 constexpr int UP_BATCH = 4;       // row/8-column units merged per thread per pass
 
+template <int UP_NR>
 __global__ void __launch_bounds__(UP_THREADS, 1)
 combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) {
+  constexpr int UP_OFF_W = up_off_w(UP_NR), UP_OFF_BAR = up_off_bar(UP_NR);
+  constexpr int kCols = up_tmem_cols(UP_NR);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -147,7 +162,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
     mbar_init(bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) { tmem_alloc(sbase + UP_OFF_BAR + 16, UP_NR); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(sbase + UP_OFF_BAR + 16, kCols); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -194,34 +209,42 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
     for (int uu = 0; uu < UP_BATCH; ++uu)
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[uu][e] = 0.f;
-    for (int s = 0; s < S; ++s) {
-      float4 x[UP_BATCH][2];
-      float ws[UP_BATCH];
+    // Two splits per step: 2 x UP_BATCH x 32 bytes of loads in flight per thread.
+    for (int s0 = 0; s0 < S; s0 += 2) {
+      float4 x[2][UP_BATCH][2];
+      float ws[2][UP_BATCH];
 #pragma unroll
-      for (int uu = 0; uu < UP_BATCH; ++uu) {
-        const int idx = base + uu * UP_THREADS;
-        const int r = idx >> 6, u = idx & 63;
-        ws[uu] = (idx < UP_NR * 64 && r < nr) ? wts[r * UP_MAX_SPLITS + s] : 0.f;
-        if (ws[uu] != 0.f) {
-          const float4* src = reinterpret_cast<const float4*>(
-              a.part_o + ((long long)s * rows + (long long)(r0 + r) * a.H + h) * 512 + 8 * u);
-          x[uu][0] = src[0];
-          x[uu][1] = src[1];
-        } else {
-          x[uu][0] = x[uu][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < 2; ++q) {
+        const int s = s0 + q;
+#pragma unroll
+        for (int uu = 0; uu < UP_BATCH; ++uu) {
+          const int idx = base + uu * UP_THREADS;
+          const int r = idx >> 6, u = idx & 63;
+          ws[q][uu] = (s < S && idx < UP_NR * 64 && r < nr) ? wts[r * UP_MAX_SPLITS + s] : 0.f;
+          if (ws[q][uu] != 0.f) {
+            const float4* src = reinterpret_cast<const float4*>(
+                a.part_o + ((long long)s * rows + (long long)(r0 + r) * a.H + h) * 512 + 8 * u);
+            x[q][uu][0] = src[0];
+            x[q][uu][1] = src[1];
+          } else {
+            x[q][uu][0] = x[q][uu][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
       }
 #pragma unroll
-      for (int uu = 0; uu < UP_BATCH; ++uu) {
-        acc[uu][0] = fmaf(ws[uu], x[uu][0].x, acc[uu][0]);
-        acc[uu][1] = fmaf(ws[uu], x[uu][0].y, acc[uu][1]);
-        acc[uu][2] = fmaf(ws[uu], x[uu][0].z, acc[uu][2]);
-        acc[uu][3] = fmaf(ws[uu], x[uu][0].w, acc[uu][3]);
-        acc[uu][4] = fmaf(ws[uu], x[uu][1].x, acc[uu][4]);
-        acc[uu][5] = fmaf(ws[uu], x[uu][1].y, acc[uu][5]);
-        acc[uu][6] = fmaf(ws[uu], x[uu][1].z, acc[uu][6]);
-        acc[uu][7] = fmaf(ws[uu], x[uu][1].w, acc[uu][7]);
-      }
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int uu = 0; uu < UP_BATCH; ++uu) {
+          const float w = ws[q][uu];
+          acc[uu][0] = fmaf(w, x[q][uu][0].x, acc[uu][0]);
+          acc[uu][1] = fmaf(w, x[q][uu][0].y, acc[uu][1]);
+          acc[uu][2] = fmaf(w, x[q][uu][0].z, acc[uu][2]);
+          acc[uu][3] = fmaf(w, x[q][uu][0].w, acc[uu][3]);
+          acc[uu][4] = fmaf(w, x[q][uu][1].x, acc[uu][4]);
+          acc[uu][5] = fmaf(w, x[q][uu][1].y, acc[uu][5]);
+          acc[uu][6] = fmaf(w, x[q][uu][1].z, acc[uu][6]);
+          acc[uu][7] = fmaf(w, x[q][uu][1].w, acc[uu][7]);
+        }
     }
 #pragma unroll
     for (int uu = 0; uu < UP_BATCH; ++uu) {
@@ -263,7 +286,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
     for (int c0 = 0; c0 < UP_NR; c0 += 32) {
       float x[32];
-      tmem_ld32(tmem + lane_addr + c0, x);
+      tmem_ld32(tmem + lane_addr + c0, x);   // columns past UP_NR (< kCols) are ignored
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -274,7 +297,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tmem, UP_NR); }
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tmem, kCols); }
 }
 
 }  // namespace
@@ -303,20 +326,44 @@ cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+namespace {
+template <int NR>
+cudaError_t launch_combine_uproj_nr(const CUtensorMap& tw, const Args& a, cudaStream_t st,
+                                    bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(combine_uproj_tc_kernel<NR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, up_smem(NR));
+  if (e != cudaSuccess) return e;
+  const unsigned nblk = (unsigned)(((long long)a.B * a.N + NR - 1) / NR);
+  return launch_ex(combine_uproj_tc_kernel<NR>, dim3(a.H, nblk), dim3(UP_THREADS), up_smem(NR),
+                   st, pdl, tw, a);
+}
+}  // namespace
+
+// Rows per CTA: the smallest of 16 / 32 / 64 whose grid (heads x row blocks)
+// still runs in one wave (one CTA per SM: W_UV[h] alone fills 128 KiB of
+// shared memory); 64 once no choice fits.  Thinner CTAs spread the partial
+// reads of small batches over more SMs; each CTA re-reads its head's W_UV,
+// mostly from L2.
+int combine_uproj_rows_per_cta(const Args& a, int sms) {
+  const long long bn = (long long)a.B * a.N;
+  for (int nr = 16; nr < 64; nr <<= 1)
+    if ((long long)a.H * ((bn + nr - 1) / nr) <= sms) return nr;
+  return 64;
+}
+
 cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t st,
                                     cudaEvent_t* ev) {
   if (!combine_uproj_tc_ok(a)) return launch_combine_uproj(a, p, st, ev);
   CUtensorMap tw;
   if (encode_2d(&tw, a.W_UV, (uint64_t)a.H * 128, 512, 64, 128) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(combine_uproj_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, UP_SMEM);
-  if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[3], st);   // the combine is fused into the up-projection
-  const unsigned nblk = (unsigned)(((long long)a.B * a.N + UP_NR - 1) / UP_NR);
   // Overlap with the attention kernel's tail unless phase events split the call.
-  e = launch_ex(combine_uproj_tc_kernel, dim3(a.H, nblk), dim3(UP_THREADS), UP_SMEM, st,
-                /*pdl=*/ev == nullptr, tw, a);
+  const bool pdl = ev == nullptr;
+  const int nr = combine_uproj_rows_per_cta(a, p.sms);
+  cudaError_t e = nr == 64 ? launch_combine_uproj_nr<64>(tw, a, st, pdl)
+                : nr == 32 ? launch_combine_uproj_nr<32>(tw, a, st, pdl)
+                           : launch_combine_uproj_nr<16>(tw, a, st, pdl);
   if (ev) cudaEventRecord(ev[4], st);
   return e;
 }
