@@ -21,20 +21,25 @@
 //
 // TMEM (512 columns per CTA): O_c [0, 256) fp32; q_lat half [256, 384) as
 // bf16 pairs (the A operand of Q.K^T); two score buffers [384, 448) and
-// [448, 512) whose first 32 columns receive P as bf16 pairs once the scores
-// have been read (the A operand of P.V).  Shared memory: a 4-stage TMA ring
-// of 64-key cache tiles (128-byte swizzled 64-column chunks; the same tile is
-// the K-major B operand of Q.K^T and the MN-major B operand of P.V), q_rope
-// (CTA 0), and two receive buffers of the score exchange.
+// [448, 512).  Shared memory: a 3-stage TMA ring of 64-key cache tiles
+// (128-byte swizzled 64-column chunks; the same tile is the K-major B operand
+// of Q.K^T and the MN-major B operand of P.V), q_rope (CTA 0), two P tiles
+// (the K-major A operand of P.V), and two receive buffers of the score
+// exchange.  Key tiles are prefetched into L2 a few tiles ahead of the ring.
 //
-// Warp roles (448 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
-// issues the MMAs; warps 2-5 (one thread per query row / TMEM lane) read each
-// partial score tile and stream it to the peer with st.async as scaled fp16;
-// warps 6-13 (two threads per row, 32 key columns each) load Q into TMEM, add
-// the peer's partial, mask, run the softmax, write P and the epilogue.  Two
-// receive buffers let the transfer of tile j+1 overlap the softmax of tile j.  Every wait is bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL);
-// on timeout the kernel records KDTV_ERR_DEVICE_TIMEOUT, drains its in-flight
-// copies and MMAs, frees TMEM and returns.
+// Warp roles (480 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
+// issues Q.K^T; warps 2-5 (one thread per query row) quantise each partial
+// score tile to fp16 once, write it back into the score buffer for their own
+// softmax and stream it to the peer with st.async; warps 6-13 (16 rows each,
+// four threads per row in the .16x256b TMEM layout, so row maxima and sums
+// meet by warp shuffles) add the peer's partial, mask, run the online
+// softmax, write P to shared memory and finally write the partial o_lat;
+// warp 14 issues P.V.  A score buffer is reused once its scores are read, so
+// Q.K^T runs up to two tiles ahead of the softmax, and two receive buffers
+// let the transfer of tile j+1 overlap the softmax of tile j.  Every wait is
+// bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL); on timeout the kernel
+// records KDTV_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs,
+// frees TMEM and returns.
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -57,15 +62,14 @@ constexpr int kPrefetch = 3;     // key tiles prefetched into L2 beyond the stag
 constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk per key tile
 constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
 constexpr int kQRopeBytes = BM * CH * 2;
-// Score exchange buffers.  A partial score row travels as 64 fp16 values,
-// each 32-column half scaled by an exact power of two chosen from that half's
-// largest magnitude (so it cannot overflow and keeps 11 significant bits
-// relative to that maximum), plus the two 32-bit exponents.  Chunk-major:
-// 16-byte chunk v of row r at (v * BM + r) * 16, so one warp store is a
-// contiguous 512-byte block; the exponents follow as [2][BM] words.
+// Score exchange buffers.  A partial score row travels as 64 fp16 values
+// scaled by an exact power of two chosen from the row's largest magnitude (so
+// it cannot overflow and keeps 11 significant bits relative to that maximum),
+// 128 bytes per row in the order the softmax threads read it, then one 32-bit
+// exponent per row.
 constexpr int kRxData = BM * BN * 2;
-constexpr int kRxBytes = kRxData + 2 * BM * 4;
-constexpr int kThreads = 480;    // TMA, QK^T issuer, 4 senders, 8 softmax (2 per row), P.V issuer
+constexpr int kRxBytes = kRxData + BM * 4;
+constexpr int kThreads = 480;    // TMA, QK^T issuer, 4 senders, 8 softmax, P.V issuer
 constexpr int kWarpPV = 14;      // the P.V issuer warp
 constexpr int kPBytes = BM * BN * 2;   // one P tile: 128 rows x 64 keys bf16, 128B-swizzled
 constexpr int kTmemCols = 512;
@@ -80,10 +84,9 @@ constexpr int OFF_P = OFF_QR + kQRopeBytes;                  // two P tiles (A o
 constexpr int OFF_RX = OFF_P + 2 * kPBytes;                   // two receive buffers
 constexpr int OFF_ANC = OFF_RX + 2 * kRxStride;
 constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 16;               // staged parent[]
-constexpr int OFF_HMAX = OFF_PAR + kMaxNodes * 4;               // [2 tiles][2 halves][BM] floats
-constexpr int OFF_LSUM = OFF_HMAX + 2 * 2 * BM * 4;             // [2 halves][BM] floats
-constexpr int OFF_OSH = OFF_LSUM + 2 * BM * 4;             // [2 tiles][2 halves][BM] own fp16 shifts
-constexpr int OFF_BAR = OFF_OSH + 2 * 2 * BM * 4;
+constexpr int OFF_LSUM = OFF_PAR + kMaxNodes * 4;               // [l | m][BM] floats (epilogue)
+constexpr int OFF_OSH = OFF_LSUM + 2 * BM * 4;                   // [2 tiles][BM] own fp16 shifts
+constexpr int OFF_BAR = OFF_OSH + 2 * BM * 4;
 constexpr int kNumBars = 40;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
@@ -106,15 +109,14 @@ enum Bar : int {
   B_TX_OK = B_RX_FULL + 2,           // [2]
   B_STALL = B_TX_OK + 2,
   B_MMA_DONE = B_STALL + 1,
-  B_HMAX = B_MMA_DONE + 1,           // [2][4] the two half-row warps of a quadrant met (tile max)
-  B_LSUM = B_HMAX + 8,               // the two half-row threads met (row sums)
+  B_LSUM = B_MMA_DONE + 1,           // softmax warps published the rows' (l, m)
   B_COUNT = B_LSUM + 1
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 
 // Wait sites (reported as the timeout detail).
 enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK, W_RX_FULL,
-            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_HMAX, W_OWN };
+            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_OWN };
 
 struct TcCfg {
   int row_tiles;               // ceil(N * H / 128)
@@ -188,7 +190,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     mbar_init(BAR(B_O_FULL), 1);
     mbar_init(BAR(B_STALL), 1);
     mbar_init(BAR(B_MMA_DONE), 2);      // both MMA issuers drained
-    for (int i = 0; i < 8; ++i) mbar_init(BAR(B_HMAX + i), 2);
     mbar_init(BAR(B_LSUM), 8);
     mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchange of tiles 0 and 1
     mbar_expect_tx(BAR(B_RX_FULL + 1), kRxBytes);
@@ -336,26 +337,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32, sv[1]);
       tmem_wait_ld();
       // Quantise the partial scores once, to fp16 with an exact power-of-two
-      // scale per 32-column half; the same words go to the peer and, through
-      // the first 32 columns of this score buffer, to our own softmax warps.
+      // scale per row; the same words go to the peer and, through the first 32
+      // columns of this score buffer, to our own softmax warps.
       uint32_t w[32];
-      int sh[2];
+      float amax = 0.f;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float amax = 0.f;
+      for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fmaxf(fabsf(sv[0][k]), fabsf(sv[1][k])));
+      const int sh = fp16_shift(amax);
+      const float sc = pow2f(sh);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fabsf(sv[hh][k]));
-        sh[hh] = fp16_shift(amax);
-        const float sc = pow2f(sh[hh]);
+      for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           __half2 h2 = __floats2half2_rn(sv[hh][2 * k] * sc, sv[hh][2 * k + 1] * sc);
           w[16 * hh + k] = *reinterpret_cast<uint32_t*>(&h2);
         }
-      }
       tmem_st32u(tmem + lane_addr + kColSP + 64 * buf, w);
-      osh[(buf * 2 + 0) * BM + r] = sh[0];
-      osh[(buf * 2 + 1) * BM + r] = sh[1];
+      osh[buf * BM + r] = sh;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -366,52 +364,62 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                                              W_TX_OK));
         if (!alive) break;
       }
-      const uint32_t rx_remote = mapa(sbase + OFF_RX + buf * kRxStride + r * 16, peer);
+      // Receive layout, chunk-major: 16-byte chunk m = 2c + h of row r at
+      // (m * BM + r) * 16 holds words {2c, 2c+1, 2c+8, 2c+9} (h = 0) or
+      // {2c+16, 2c+17, 2c+24, 2c+25} (h = 1), the words one .16x256b softmax
+      // thread (c = t % 4) needs; one warp store is a contiguous 512-byte
+      // block.  The rows' shifts follow the data.
+      const uint32_t rx_row = mapa(sbase + OFF_RX + buf * kRxStride + r * 16, peer);
       const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL + buf), peer);
 #pragma unroll
-      for (int v = 0; v < 8; ++v)
-        st_async_v4u(rx_remote + v * BM * 16, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3],
-                     rxfull_remote);
+      for (int cq = 0; cq < 4; ++cq)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-        st_async_u32(mapa(sbase + OFF_RX + buf * kRxStride + kRxData + (hh * BM + r) * 4, peer),
-                     (uint32_t)sh[hh], rxfull_remote);
+        for (int h = 0; h < 2; ++h) {
+          const int w0 = 2 * cq + 16 * h;
+          st_async_v4u(rx_row + (2 * cq + h) * BM * 16, w[w0], w[w0 + 1], w[w0 + 8], w[w0 + 9],
+                       rxfull_remote);
+        }
+      st_async_u32(mapa(sbase + OFF_RX + buf * kRxStride + kRxData + r * 4, peer), (uint32_t)sh,
+                   rxfull_remote);
     }
   } else if (warp < kWarpPV) {
-    // ---- softmax warps 6..13: two threads per query row, 32 key columns each --------------
-    const int q = warp & 3;                      // TMEM lane quadrant of this warp
-    const int hh = (warp - 6) >> 2;              // which half of the 64 key columns
-    const int r = q * 32 + lane;                 // row within the tile = TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    const int rr = rt * BM + r;                  // row within the request
-    const bool row_valid = rr < a.N * a.H;
-    const int node = row_valid ? rr / a.H : 0;
-    uint32_t an0 = 0, an1 = 0, an2 = 0, an3 = 0;
-    if (ok && row_valid) {
-      an0 = anc[4 * node]; an1 = anc[4 * node + 1]; an2 = anc[4 * node + 2]; an3 = anc[4 * node + 3];
-    }
+    // ---- softmax warps 6..13 ------------------------------------------------------------
+    // Warp (q, g) owns tile rows 32q + 16g .. +15 (TMEM lane quadrant q).  In the
+    // .16x256b layout thread t holds rows ra = base + t/4 and rb = ra + 8, keys
+    // 16k + 4c .. 16k + 4c + 3 (c = t % 4, k = 0..3) of each 64-key tile, so the
+    // four threads of a row meet through two shuffles.
+    const int q = warp & 3;
+    const int g = (warp - 6) >> 2;
+    const int c = lane & 3;
+    const int ra = 32 * q + 16 * g + (lane >> 2), rb = ra + 8;
+    const uint32_t lane16 = static_cast<uint32_t>(32 * q + 16 * g) << 16;
+    const uint32_t lane32 = static_cast<uint32_t>(32 * q) << 16;
+    const int nrows = a.N * a.H;
+    const bool va = rt * BM + ra < nrows, vb = rt * BM + rb < nrows;
     const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
-    float* hmax = reinterpret_cast<float*>(sm + OFF_HMAX);
     float* lsum = reinterpret_cast<float*>(sm + OFF_LSUM);
     const int* osh = reinterpret_cast<const int*>(sm + OFF_OSH);
-    float m_used = -INFINITY, l_half = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
     bool alive = true;
 
     if (nt > 0) {
       grid_dep_wait();   // q_lat is written by the absorb kernel
-      // this thread's 64 bf16 pairs of the q_lat half -> TMEM [kColQ + 64 hh, +64)
+      // Q half of tile row 32q + lane, latent columns 128g .. 128g+127 of this
+      // CTA's half -> TMEM [kColQ + 64g, +64) as bf16 pairs (.32x32b layout).
+      const int rq = rt * BM + 32 * q + lane;
+      const bool vq = rq < nrows;
       const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const __nv_bfloat16*>(a.q_lat) + (req_row0 + (row_valid ? rr : 0)) * 512 +
-          rank * kHalf + 128 * hh);
+          static_cast<const __nv_bfloat16*>(a.q_lat) + (req_row0 + (vq ? rq : 0)) * 512 +
+          rank * kHalf + 128 * g);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int h = 0; h < 2; ++h) {
         uint32_t w[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          uint4 x = row_valid ? src[8 * c + v] : make_uint4(0u, 0u, 0u, 0u);
+          uint4 x = vq ? src[8 * h + v] : make_uint4(0u, 0u, 0u, 0u);
           w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
         }
-        tmem_st32u(tmem + lane_addr + kColQ + 64 * hh + 32 * c, w);
+        tmem_st32u(tmem + lane32 + kColQ + 64 * g + 32 * h, w);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -428,98 +436,120 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       alive = __all_sync(0xffffffffu, wait(BAR(B_OWN + buf), (j >> 1) & 1, st, limit, W_OWN));
       if (!alive) break;
       tc_fence_after();
-      // own partial scores of this half: 16 fp16 pairs written by the sender warps
+      // own quantised partial scores (fp16 pairs, columns 0..31 of the score buffer)
       uint32_t ow[16];
-      tmem_ld16u(tmem + lane_addr + kColSP + 64 * buf + 16 * hh, ow);
-      const int own_sh = osh[(buf * 2 + hh) * BM + r];
+      tmem_ld_16x256b_x4(tmem + lane16 + kColSP + 64 * buf, ow);
+      const float oia = pow2f(-osh[buf * BM + ra]), oib = pow2f(-osh[buf * BM + rb]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));   // QK^T of tile j+2 may overwrite
 
-      // + the peer's partial scores for these columns (its st.async filled rx[buf]).
-      // Both products are exact (fp16 times a power of two), so own + peer
-      // rounds to the same float in both CTAs whichever is added first.
+      // + the peer's partial scores (its st.async filled rx[buf]).  Both products
+      // are exact (fp16 times a power of two), so own + peer rounds to the same
+      // float in both CTAs whichever is added first.
       alive = __all_sync(0xffffffffu,
                          wait<true>(BAR(B_RX_FULL + buf), (j >> 1) & 1, st, limit, W_RX_FULL));
       if (!alive) break;
       consumed = j + 1;
-      if (r == 0 && hh == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
-      float sv[32];
+      if (warp == 6 && lane == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
+      float sa[16], sb[16];
       {
         const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
-        int psh;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(psh)
-                     : "r"(rxb + kRxData + (hh * BM + r) * 4) : "memory");
-        const float pinv = pow2f(-psh), oinv = pow2f(-own_sh);
+        int psa, psb;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(psa) : "r"(rxb + kRxData + ra * 4) : "memory");
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(psb) : "r"(rxb + kRxData + rb * 4) : "memory");
+        const float pia = pow2f(-psa), pib = pow2f(-psb);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint32_t w[4];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                       : "r"(rxb + ((4 * hh + v) * BM + r) * 16) : "memory");
+        for (int rsel = 0; rsel < 2; ++rsel) {
+          const int row = rsel ? rb : ra;
+          const float pinv = rsel ? pib : pia, oinv = rsel ? oib : oia;
+          float* sv = rsel ? sb : sa;
+          uint32_t pw[8];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 fp = __half22float2(*reinterpret_cast<__half2*>(&w[u]));
-            const float2 fo = __half22float2(*reinterpret_cast<__half2*>(&ow[4 * v + u]));
-            sv[8 * v + 2 * u] = fmaf(fp.x, pinv, fo.x * oinv);
-            sv[8 * v + 2 * u + 1] = fmaf(fp.y, pinv, fo.y * oinv);
-          }
+          for (int h = 0; h < 2; ++h)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(pw[4 * h]), "=r"(pw[4 * h + 1]), "=r"(pw[4 * h + 2]),
+                           "=r"(pw[4 * h + 3])
+                         : "r"(rxb + ((2 * c + h) * BM + row) * 16) : "memory");
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              // key 16k + 4c + 2e (+1): own word ow[4k + 2 rsel + e], peer word pw[2k + e]
+              const float2 fo = __half22float2(*reinterpret_cast<const __half2*>(&ow[4 * k + 2 * rsel + e]));
+              const float2 fp = __half22float2(*reinterpret_cast<const __half2*>(&pw[2 * k + e]));
+              sv[4 * k + 2 * e] = fmaf(fp.x, pinv, fo.x * oinv);
+              sv[4 * k + 2 * e + 1] = fmaf(fp.y, pinv, fo.y * oinv);
+            }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));  // consumed
 
-      // visibility mask (only tiles that reach past the prefix)
-      const int t0 = k0 + j * BN + 32 * hh;
-      if (!(row_valid && t0 + 32 <= L)) {
+      // visibility mask (only tiles that reach past the prefix, or rows past the end)
+      const int tb = k0 + j * BN;
+      if (!(va && vb && tb + BN <= L)) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int t = t0 + k;
-          bool vis = false;
-          if (row_valid && t < k1) {
-            if (t < L) {
-              vis = true;
-            } else {
-              const int jn = t - L;
-              const uint32_t w = jn < 32 ? an0 : jn < 64 ? an1 : jn < 96 ? an2 : an3;
-              vis = (w >> (jn & 31)) & 1u;
+        for (int rsel = 0; rsel < 2; ++rsel) {
+          const bool vrow = rsel ? vb : va;
+          const int node = vrow ? (rt * BM + (rsel ? rb : ra)) / a.H : 0;
+          float* sv = rsel ? sb : sa;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int t = tb + 16 * k + 4 * c + e;
+              bool vis = false;
+              if (vrow && t < k1) {
+                if (t < L) {
+                  vis = true;
+                } else {
+                  const int jn = t - L;
+                  vis = (anc[4 * node + (jn >> 5)] >> (jn & 31)) & 1u;
+                }
+              }
+              if (!vis) sv[4 * k + e] = -INFINITY;
             }
-          }
-          if (!vis) sv[k] = -INFINITY;
         }
       }
-      // tile max of the full row: the two half-row threads meet (bounded wait)
-      hmax[(buf * 2 + hh) * BM + r] = max32(sv);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_HMAX + 4 * buf + q));
-      alive = __all_sync(0xffffffffu,
-                         wait(BAR(B_HMAX + 4 * buf + q), (j >> 1) & 1, st, limit, W_HMAX));
-      if (!alive) break;
-      const float m_tile =
-          fmaxf(hmax[(buf * 2) * BM + r], hmax[(buf * 2 + 1) * BM + r]) * sl2;
+      // row maxima: 16 keys per thread, then the row's four threads
+      float mta = sa[0], mtb = sb[0];
+#pragma unroll
+      for (int k = 1; k < 16; ++k) { mta = fmaxf(mta, sa[k]); mtb = fmaxf(mtb, sb[k]); }
+      mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 1));
+      mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 1));
+      mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 2)) * sl2;
+      mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 2)) * sl2;
 
       // lazy rescale: move the reference max only when it grows by > 8 (log2);
-      // both half-row threads take the same decision from the same inputs
-      float alpha = 1.f;
+      // the four threads of a row take the same decision from the same inputs
+      float alpha_a = 1.f, alpha_b = 1.f;
       bool rescale = false;
-      if (m_tile > m_used + 8.f) {
-        if (m_used != -INFINITY) { alpha = ex2(m_used - m_tile); rescale = true; }
-        l_half *= alpha;
-        m_used = m_tile;
+      if (mta > m_a + 8.f) {
+        if (m_a != -INFINITY) { alpha_a = ex2(m_a - mta); rescale = true; }
+        l_a *= alpha_a;
+        m_a = mta;
       }
-      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-      uint32_t packed[16];
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      if (mtb > m_b + 8.f) {
+        if (m_b != -INFINITY) { alpha_b = ex2(m_b - mtb); rescale = true; }
+        l_b *= alpha_b;
+        m_b = mtb;
+      }
+      const float nma = m_a == -INFINITY ? 0.f : -m_a, nmb = m_b == -INFINITY ? 0.f : -m_b;
+      uint32_t pk[16];                            // [row][k][pair]: bf16 pairs of P
+      float psa = 0.f, psb = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        const float p0 = ex2(fmaf(sv[k], sl2, neg_m));
-        const float p1 = ex2(fmaf(sv[k + 1], sl2, neg_m));
-        const uint32_t h2 = pack_bf16x2(p0, p1);
-        packed[k >> 1] = h2;
-        ps[(k >> 1) & 3] += __uint_as_float(h2 << 16) + __uint_as_float(h2 & 0xffff0000u);
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t ha = pack_bf16x2(ex2(fmaf(sa[2 * k], sl2, nma)), ex2(fmaf(sa[2 * k + 1], sl2, nma)));
+        const uint32_t hb = pack_bf16x2(ex2(fmaf(sb[2 * k], sl2, nmb)), ex2(fmaf(sb[2 * k + 1], sl2, nmb)));
+        pk[k] = ha;
+        pk[8 + k] = hb;
+        psa += __uint_as_float(ha << 16) + __uint_as_float(ha & 0xffff0000u);
+        psb += __uint_as_float(hb << 16) + __uint_as_float(hb & 0xffff0000u);
       }
-      l_half += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      l_a += psa;
+      l_b += psb;
 
       // the P buffer is free once P.V of tile j-2 (same buffer) has completed;
       // O is stable once P.V of tile j-1 has completed
@@ -535,29 +565,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           if (!alive) break;
         }
         tc_fence_after();
-        for (int c = 0; c < kHalf / 64; ++c) {        // this thread's 128 of the 256 O columns
-          float ov[32];
-          const uint32_t oa = tmem + lane_addr + kColO + 128 * hh + 32 * c;
-          tmem_ld32(oa, ov);
+        for (int cc = 0; cc < kHalf / 64; ++cc) {     // this warp's 16 rows x 256 O columns
+          uint32_t ov[32];
+          const uint32_t oa = tmem + lane16 + kColO + 64 * cc;
+          tmem_ld_16x256b_x8(oa, ov);
           tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) ov[k] *= alpha;
-          tmem_st32(oa, ov);
+          for (int k = 0; k < 8; ++k) {
+            ov[4 * k] = __float_as_uint(__uint_as_float(ov[4 * k]) * alpha_a);
+            ov[4 * k + 1] = __float_as_uint(__uint_as_float(ov[4 * k + 1]) * alpha_a);
+            ov[4 * k + 2] = __float_as_uint(__uint_as_float(ov[4 * k + 2]) * alpha_b);
+            ov[4 * k + 3] = __float_as_uint(__uint_as_float(ov[4 * k + 3]) * alpha_b);
+          }
+          tmem_st_16x256b_x8(oa, ov);
         }
         tmem_wait_st();
         tc_fence_before();
       }
-      // P row r, keys 32hh..32hh+31 = 16-byte chunks 4hh..4hh+3 of the row's 128
-      // bytes, stored 128B-swizzled (chunk c of row r at c ^ (r & 7)): the
-      // K-major A operand layout of P.V.
+      // P rows ra, rb: keys 16k + 4c .. +3 are 8 bytes at offset 8(c & 1) of the
+      // row's 16-byte chunk 2k + c/2, stored 128B-swizzled (chunk m of row r at
+      // m ^ (r & 7)): the K-major A operand layout of P.V.
       {
-        const uint32_t prow = sbase + OFF_P + buf * kPBytes + (r >> 3) * 1024 + (r & 7) * 128;
+        const uint32_t pb = sbase + OFF_P + buf * kPBytes;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const uint32_t dst = prow + (((4 * hh + v) ^ (r & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                       :: "r"(dst), "r"(packed[4 * v]), "r"(packed[4 * v + 1]),
-                          "r"(packed[4 * v + 2]), "r"(packed[4 * v + 3]) : "memory");
+        for (int rsel = 0; rsel < 2; ++rsel) {
+          const int row = rsel ? rb : ra;
+          const uint32_t prow = pb + (row >> 3) * 1024 + (row & 7) * 128 + 8 * (c & 1);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            asm volatile("st.shared.v2.b32 [%0], {%1, %2};"
+                         :: "r"(prow + (((2 * k + (c >> 1)) ^ (row & 7)) << 4)),
+                            "r"(pk[8 * rsel + 2 * k]), "r"(pk[8 * rsel + 2 * k + 1]) : "memory");
         }
       }
       fence_async_smem();                         // visible to the tensor core
@@ -571,39 +609,52 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       drain_wait(BAR(B_RX_FULL + (t & 1)), (t >> 1) & 1, 200000ull);
 
     // ---- epilogue: unnormalised partial o_lat half, (m, l) -----------------------------
+    // Row sums meet across the row's four threads; the (m, l) of every row go
+    // through shared memory to the .32x32b read-out below (thread = row
+    // 32q + lane, O columns 128g .. 128g+127).
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
     if (alive && nt > 0)
       alive = __all_sync(0xffffffffu, wait(BAR(B_O_FULL), 0, st, limit, W_O_FULL));
-    float l_sum = 0.f;
+    float l_sum = 0.f, m_row = -INFINITY;
+    const int r = 32 * q + lane;                 // read-out row
+    const int rr = rt * BM + r;
+    const bool row_valid = rr < nrows;
     if (alive && nt > 0) {
-      lsum[hh * BM + r] = l_half;
+      if (c == 0) {
+        lsum[ra] = l_a; lsum[BM + ra] = m_a;
+        lsum[rb] = l_b; lsum[BM + rb] = m_b;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_LSUM));
       alive = __all_sync(0xffffffffu, wait(BAR(B_LSUM), 0, st, limit, W_O_FULL));
-      if (alive) l_sum = lsum[r] + lsum[BM + r];
+      if (alive) { l_sum = lsum[r]; m_row = lsum[BM + r]; }
     }
     // tcgen05.ld is warp-collective: every lane loads, only valid rows store.
     const bool has_data = ok && alive && nt > 0 && row_valid && l_sum > 0.f;
-    if (ok && alive && row_valid && hh == 0) {
+    if (ok && alive && row_valid && g == 0) {
       const long long rows = (long long)a.B * a.N * a.H;
       float* ml = a.part_ml + ((long long)s * rows + req_row0 + rr) * 2;
       if (rank == 0) {
-        ml[0] = has_data ? m_used * 0.6931471805599453f : -INFINITY;
+        ml[0] = has_data ? m_row * 0.6931471805599453f : -INFINITY;
         ml[1] = has_data ? l_sum : 0.f;
       }
     }
     if (ok && alive && nt > 0 && __any_sync(0xffffffffu, has_data)) {
       const long long rows = (long long)a.B * a.N * a.H;
       float* po = a.part_o + ((long long)s * rows + req_row0 + (has_data ? rr : 0)) * a.d_c +
-                  rank * kHalf + 128 * hh;
+                  rank * kHalf + 128 * g;
       tc_fence_after();
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
         float ov[32];
-        tmem_ld32(tmem + lane_addr + kColO + 128 * hh + 32 * c, ov);
+        tmem_ld32(tmem + lane32 + kColO + 128 * g + 32 * cc, ov);
         tmem_wait_ld();
         if (has_data) {
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(po + 32 * c + k) =
+            *reinterpret_cast<float4*>(po + 32 * cc + k) =
                 make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
         }
       }
