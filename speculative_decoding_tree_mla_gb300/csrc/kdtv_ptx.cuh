@@ -93,6 +93,16 @@ __device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t a,
                :: "r"(cluster_addr), "r"(a), "r"(cluster_bar) : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory into another CTA's; completion is counted
+// (complete_tx) on that CTA's mbarrier `cluster_bar`.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta,
+                                                  uint32_t bytes, uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst_cluster), "r"(src_cta), "r"(bytes), "r"(cluster_bar) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile("{\n\t.reg .pred p;\n\t"
@@ -111,23 +121,46 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// Bounded wait: spins until the phase with `parity` completes, the
-// time limit passes, or another CTA raised the abort flag.  On timeout it
-// records KDTV_ERR_DEVICE_TIMEOUT (detail = `site`).  Returns false if the
-// caller must abandon its work.
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until it completes or about `hint_ns` pass, instead of spinning and
+// taking issue slots from the working warps of its sub-partition.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity,
+                                                            uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: sleeps (try_wait with a 20 us suspend hint) until the phase
+// with `parity` completes, the time limit passes, or another CTA raised the
+// abort flag.  On timeout it records KDTV_ERR_DEVICE_TIMEOUT (detail =
+// `site`).  Returns false if the caller must abandon its work.
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, DeviceStatus* st,
                                      uint64_t limit_ns, uint32_t site) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0u) {
-      if (*reinterpret_cast<volatile unsigned int*>(&st->abort)) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        record_error(st, KDTV_ERR_DEVICE_TIMEOUT, site);
-        return false;
-      }
+  for (;;) {
+    if (kCluster ? mbar_try_wait_cluster_sleep(bar, parity, 20000u)
+                 : mbar_try_wait_sleep(bar, parity, 20000u))
+      return true;
+    if (*reinterpret_cast<volatile unsigned int*>(&st->abort)) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      record_error(st, KDTV_ERR_DEVICE_TIMEOUT, site);
+      return false;
     }
   }
 }
@@ -212,6 +245,14 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
                :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
                : "memory");
+}
+
+// Arrive on the mbarrier at offset `bar` in every CTA of `cta_mask` once
+// every tcgen05 op this thread issued so far completes.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" :: "r"(bar), "h"(cta_mask) : "memory");
 }
 
 // Arrive on `bar` once every tcgen05 op this thread issued so far completes.

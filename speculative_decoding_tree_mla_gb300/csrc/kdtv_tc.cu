@@ -13,33 +13,37 @@
 // the latent dimension:
 //   CTA 0 holds q_lat[:, 0:256] and q_rope, and reads c_kv[:, 0:256] + k_rope;
 //   CTA 1 holds q_lat[:, 256:512] and reads c_kv[:, 256:512].
-// Each CTA computes a partial score tile S_c = Q_c K_c^T on tcgen05 into TMEM,
-// the two partials are exchanged through distributed shared memory and
-// summed, both CTAs run the same online softmax on S = S_0 + S_1 (so they
-// agree bit for bit), and each accumulates its own half of the latent output
-// O_c += P . c_kv[:, 256c : 256c+256] in TMEM.
+// Per 64-key tile each CTA computes the partial score tile S_c = Q_c K_c^T
+// (all 128 rows) on tcgen05 into TMEM and accumulates its own half of the
+// latent output, O_c += P . c_kv[:, 256c : 256c+256] (all 128 rows).
+//
+// The softmax rows are split between the pair: CTA c owns the rows in TMEM
+// lanes 32q + 16c .. 32q + 16c + 15 of each lane quadrant q.  For every tile
+// a CTA sends the peer the peer's rows of its partial scores (fp16, one exact
+// power-of-two scale per row), adds the peer's partial for its own rows to its
+// exact fp32 partial, runs the online softmax of its own rows, and returns the
+// P rows (bf16, one 2 KiB bulk copy per quadrant) so that both CTAs hold the
+// full P tile for their P . V.  When a row's reference maximum moves, its
+// owner also sends the rescale factor, and each CTA rescales its half of O.
 //
 // TMEM (512 columns per CTA): O_c [0, 256) fp32; q_lat half [256, 384) as
 // bf16 pairs (the A operand of Q.K^T); two score buffers [384, 448) and
-// [448, 512).  Shared memory: a 3-stage TMA ring of 64-key cache tiles
+// [448, 512).  Shared memory: a 4-stage TMA ring of 64-key cache tiles
 // (128-byte swizzled 64-column chunks; the same tile is the K-major B operand
-// of Q.K^T and the MN-major B operand of P.V), q_rope (CTA 0), two P tiles
-// (the K-major A operand of P.V), and two receive buffers of the score
-// exchange.  Key tiles are prefetched into L2 a few tiles ahead of the ring.
+// of Q.K^T and the MN-major B operand of P.V), q_rope (CTA 0), the P tile
+// (K-major A operand of P.V), two receive buffers for the peer's scores and
+// four for its rescale factors.  Key tiles are also prefetched into L2 a few
+// tiles ahead of the ring.
 //
-// Warp roles (480 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
-// issues Q.K^T; warps 2-5 (one thread per query row) quantise each partial
-// score tile to fp16 once, write it back into the score buffer for their own
-// softmax and stream it to the peer with st.async; warps 6-13 (16 rows each,
-// four threads per row in the .16x256b TMEM layout, so row maxima and sums
-// meet by warp shuffles) add the peer's partial, mask, run the online
-// softmax, write P to shared memory and finally write the partial o_lat;
-// warp 14 issues P.V.  A score buffer is reused once its scores are read, so
-// Q.K^T runs up to two tiles ahead of the softmax, and two receive buffers
-// let the transfer of tile j+1 overlap the softmax of tile j.  Every wait is
-// bounded (2 s, or ~20 ms with KDTV_FLAG_TEST_STALL); on timeout the kernel
-// records KDTV_ERR_DEVICE_TIMEOUT, drains its in-flight copies and MMAs,
-// frees TMEM and returns.
+// Warp roles (352 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
+// issues Q.K^T; warps 2-5 (one per lane quadrant) quantise and send the
+// peer's score rows; warps 6-9 (one per quadrant, four threads per row in
+// the .16x256b TMEM layout, so row maxima and sums meet by warp shuffles) run
+// the softmax of the CTA's own rows; warp 10 issues P.V.  Warps 2-9 also load
+// Q into TMEM and write the partial o_lat.  Every wait is bounded (2 s, or
+// ~20 ms with KDTV_FLAG_TEST_STALL); on timeout the kernel records
+// KDTV_ERR_DEVICE_TIMEOUT, lets in-flight copies land, drains its MMAs, frees
+// TMEM and returns.
 
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -57,66 +61,69 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 64;           // keys per tile (MMA N of Q.K^T)
 constexpr int CH = 64;           // bf16 columns per 128-byte swizzled chunk
 constexpr int kHalf = 256;       // latent columns per CTA
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kPrefetch = 3;     // key tiles prefetched into L2 beyond the stages in flight
 constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk per key tile
 constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
 constexpr int kQRopeBytes = BM * CH * 2;
-// Score exchange buffers.  A partial score row travels as 64 fp16 values
-// scaled by an exact power of two chosen from the row's largest magnitude (so
-// it cannot overflow and keeps 11 significant bits relative to that maximum),
-// 128 bytes per row in the order the softmax threads read it, then one 32-bit
-// exponent per row.
-constexpr int kRxData = BM * BN * 2;
-constexpr int kRxBytes = kRxData + BM * 4;
-constexpr int kThreads = 480;    // TMA, QK^T issuer, 4 senders, 8 softmax, P.V issuer
-constexpr int kWarpPV = 14;      // the P.V issuer warp
-constexpr int kPBytes = BM * BN * 2;   // one P tile: 128 rows x 64 keys bf16, 128B-swizzled
+constexpr int kPBytes = BM * BN * 2;    // the P tile: 128 rows x 64 keys bf16, 128B-swizzled
+constexpr int kPQuadBytes = 16 * BN * 2;   // one quadrant's own P rows (contiguous, 2 KiB)
+// Score exchange: the peer's 64 rows as fp16 in the receiving softmax
+// thread's order: 16-byte chunk m (0..3) of thread t of quadrant q at
+// ((q * 4 + m) * 32 + t) * 16, so one warp store is a contiguous 512-byte
+// block; then one word per (q, t) holding its two rows' shifts.
+constexpr int kRxData = 4 * 4 * 32 * 16;
+constexpr int kRxBytes = kRxData + 4 * 32 * 4;
+constexpr int kRxStride = (kRxBytes + 127) / 128 * 128;
+constexpr int kAfBufs = 4;              // rescale-factor buffers, [BM] floats each
+constexpr int kAfBytes = 64 * 4;        // the peer's 64 rows per tile
+constexpr int kThreads = 352;
+constexpr int kWarpPV = 10;
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;
 constexpr int kColQ = 256;
-constexpr int kColSP = 384;      // + 64 * buffer
+constexpr int kColS = 384;       // + 64 * buffer
 
 constexpr int OFF_KV = 0;
 constexpr int OFF_QR = OFF_KV + kStages * kMaxCh * kKVChunk;
-constexpr int kRxStride = (kRxBytes + 1023) / 1024 * 1024;
-constexpr int OFF_P = OFF_QR + kQRopeBytes;                  // two P tiles (A of P.V)
-constexpr int OFF_RX = OFF_P + 2 * kPBytes;                   // two receive buffers
-constexpr int OFF_ANC = OFF_RX + 2 * kRxStride;
-constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 16;               // staged parent[]
-constexpr int OFF_LSUM = OFF_PAR + kMaxNodes * 4;               // [l | m][BM] floats (epilogue)
-constexpr int OFF_OSH = OFF_LSUM + 2 * BM * 4;                   // [2 tiles][BM] own fp16 shifts
-constexpr int OFF_BAR = OFF_OSH + 2 * BM * 4;
-constexpr int kNumBars = 40;
+constexpr int OFF_P = OFF_QR + kQRopeBytes;
+constexpr int OFF_RX = OFF_P + kPBytes;                        // two receive buffers
+constexpr int OFF_AF = OFF_RX + 2 * kRxStride;                 // [kAfBufs][BM] floats
+constexpr int OFF_ANC = OFF_AF + kAfBufs * BM * 4;
+constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 16;              // staged parent[]
+constexpr int OFF_BAR = OFF_PAR + kMaxNodes * 4;
+constexpr int kNumBars = 32;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(OFF_P % 1024 == 0 && OFF_RX % 1024 == 0 && OFF_QR % 1024 == 0,
-              "128B-swizzled tiles need 1 KiB alignment");
+static_assert(OFF_QR % 1024 == 0 && OFF_P % 1024 == 0, "128B-swizzled tiles need 1 KiB alignment");
+static_assert(OFF_RX % 16 == 0 && kRxStride % 16 == 0 && OFF_AF % 16 == 0, "async store alignment");
 static_assert(kThreads == 32 * (kWarpPV + 1), "warp roles");
 
 // Barrier indices (derived from kStages so the groups never overlap).
 enum Bar : int {
-  B_QR_FULL = 0, B_Q_READY = 1, B_KV_FULL = 2,
-  B_KV_EMPTY = B_KV_FULL + kStages,
-  B_S_FULL = B_KV_EMPTY + kStages,   // [2]
-  B_S_FREE = B_S_FULL + 2,           // [2] the softmax has read the quantised own scores
-  B_OWN = B_S_FREE + 2,              // [2] senders wrote the quantised own scores
-  B_P_FULL = B_OWN + 2,              // [2]
-  B_P_EMPTY = B_P_FULL + 2,          // [2]
-  B_O_FULL = B_P_EMPTY + 2,
-  B_RX_FULL = B_O_FULL + 1,          // [2]
-  B_TX_OK = B_RX_FULL + 2,           // [2]
-  B_STALL = B_TX_OK + 2,
-  B_MMA_DONE = B_STALL + 1,
-  B_LSUM = B_MMA_DONE + 1,           // softmax warps published the rows' (l, m)
-  B_COUNT = B_LSUM + 1
+  B_QR_FULL = 0,
+  B_Q_READY = 1,                     // 8 warps stored their part of Q in TMEM
+  B_KV_FULL = 2,                     // [kStages]
+  B_KV_EMPTY = B_KV_FULL + kStages,  // [kStages]
+  B_S_FULL = B_KV_EMPTY + kStages,   // [2] Q.K^T of the tile completed
+  B_S_FREE = B_S_FULL + 2,           // [2] senders and softmax read the scores
+  B_RX_FULL = B_S_FREE + 2,          // [2] the peer's score rows landed (tx)
+  B_TX_OK = B_RX_FULL + 2,           // [2] the peer consumed what we sent (remote)
+  B_AF_FULL = B_TX_OK + 2,           // [kAfBufs] the peer's rescale factors landed (tx)
+  B_P_FULL = B_AF_FULL + kAfBufs,    // our softmax wrote its P rows
+  B_P_RX = B_P_FULL + 1,             // the peer's P rows landed (tx)
+  B_P_EMPTY = B_P_RX + 1,            // P.V of the tile completed in both CTAs
+  B_O_FULL = B_P_EMPTY + 1,
+  B_MMA_DONE = B_O_FULL + 1,         // both MMA issuers drained
+  B_STALL = B_MMA_DONE + 1,
+  B_COUNT = B_STALL + 1
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 
 // Wait sites (reported as the timeout detail).
 enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK, W_RX_FULL,
-            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_OWN };
+            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_AF, W_P_RX };
 
 struct TcCfg {
   int row_tiles;               // ceil(N * H / 128)
@@ -128,7 +135,7 @@ __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t
 
 // Shift that maps max |v| into [2^14, 2^15): the fp16 range with headroom.
 // Capped at 100 so that every nonzero fp16 value times 2^-shift is a normal
-// float: the dequantised products are then exact in both CTAs.
+// float.
 __device__ __forceinline__ int fp16_shift(float amax) {
   if (!(amax > 0.f)) return 0;
   const int e = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;   // floor(log2(amax))
@@ -136,15 +143,30 @@ __device__ __forceinline__ int fp16_shift(float amax) {
   return sh < -126 ? -126 : (sh > 100 ? 100 : sh);
 }
 
-__device__ __forceinline__ float max32(const float (&v)[32]) {
-  float m[16];
+// Three-input maximum (one instruction on sm_100-class GPUs).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Scale 16 O rows (a .16x256b warp slice: rows base + t/4 and base + t/4 + 8)
+// of this CTA's 256 O columns by alpha_a / alpha_b.
+__device__ __forceinline__ void rescale_o_rows(uint32_t taddr, float alpha_a, float alpha_b) {
+#pragma unroll 1
+  for (int cc = 0; cc < kHalf / 64; ++cc) {
+    uint32_t ov[32];
+    tmem_ld_16x256b_x8(taddr + 64 * cc, ov);
+    tmem_wait_ld();
 #pragma unroll
-  for (int i = 0; i < 16; ++i) m[i] = fmaxf(v[2 * i], v[2 * i + 1]);
-#pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
-  return m[0];
+    for (int k = 0; k < 8; ++k) {
+      ov[4 * k] = __float_as_uint(__uint_as_float(ov[4 * k]) * alpha_a);
+      ov[4 * k + 1] = __float_as_uint(__uint_as_float(ov[4 * k + 1]) * alpha_a);
+      ov[4 * k + 2] = __float_as_uint(__uint_as_float(ov[4 * k + 2]) * alpha_b);
+      ov[4 * k + 3] = __float_as_uint(__uint_as_float(ov[4 * k + 3]) * alpha_b);
+    }
+    tmem_st_16x256b_x8(taddr + 64 * cc, ov);
+  }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -180,19 +202,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(B_S_FULL + i), 1);
-      mbar_init(BAR(B_S_FREE + i), 8);    // 8 softmax warps have read the own scores
-      mbar_init(BAR(B_OWN + i), 4);       // 4 sender warps quantised them
-      mbar_init(BAR(B_P_FULL + i), 8);
-      mbar_init(BAR(B_P_EMPTY + i), 1);
+      mbar_init(BAR(B_S_FREE + i), 8);    // 4 sender + 4 softmax warps read the scores
       mbar_init(BAR(B_RX_FULL + i), 1);   // armed with expect_tx; filled by the peer's st.async
-      mbar_init(BAR(B_TX_OK + i), 8);     // one relaxed arrival per peer softmax warp
+      mbar_init(BAR(B_TX_OK + i), 4);     // one relaxed arrival per peer softmax warp
     }
+    for (int i = 0; i < kAfBufs; ++i) mbar_init(BAR(B_AF_FULL + i), 1);
+    mbar_init(BAR(B_P_FULL), 4);          // our 4 softmax warps
+    mbar_init(BAR(B_P_RX), 1);            // armed with expect_tx; filled by the peer's bulk copies
+    mbar_init(BAR(B_P_EMPTY), 2);         // P.V commits of both CTAs (multicast)
     mbar_init(BAR(B_O_FULL), 1);
+    mbar_init(BAR(B_MMA_DONE), 2);
     mbar_init(BAR(B_STALL), 1);
-    mbar_init(BAR(B_MMA_DONE), 2);      // both MMA issuers drained
-    mbar_init(BAR(B_LSUM), 8);
-    mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchange of tiles 0 and 1
+    mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchanges of tiles 0 and 1
     mbar_expect_tx(BAR(B_RX_FULL + 1), kRxBytes);
+    for (int i = 0; i < kAfBufs; ++i) mbar_expect_tx(BAR(B_AF_FULL + i), kAfBytes);
+    mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes);
     fence_mbar_init();
     int L = 0;
     int ok = prefix_ok(a, b, &L) ? 1 : 0;
@@ -229,7 +253,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();   // the peer's barriers are initialised before any remote arrive
+  cluster_sync();   // the peer's barriers are initialised before any remote access
 
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const bool ok = misc[1] && misc[3];
@@ -239,6 +263,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
   const int k1 = min(T, k0 + a.chunk);
   const int nt = (ok && k1 > k0) ? (k1 - k0 + BN - 1) / BN : 0;
   const long long req_row0 = (long long)b * a.N * a.H;    // first global row of request b
+  const int nrows = a.N * a.H;
 
   if (warp == 0) {
     // ---- TMA producer --------------------------------------------------------------
@@ -255,8 +280,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         return a.page_size ? a.page_table[(long long)b * a.max_pages + t0 / a.page_size] * a.page_size
                            : b * a.t_stride + t0;
       };
-      // L2 prefetch kPrefetch tiles ahead of the loads, so that a refilled
-      // stage finds its tile in L2 rather than in DRAM.
       auto prefetch = [&](int j) {
         const int row = tile_row(j);
         for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_ckv, (int)rank * kHalf + c * CH, row);
@@ -299,7 +322,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           alive = wait(BAR(B_S_FREE + buf), ((j >> 1) - 1) & 1, st, limit, W_S_FREE);
         if (!alive) break;
         tc_fence_after();
-        const uint32_t d = tmem + kColSP + 64 * buf;
+        const uint32_t d = tmem + kColS + 64 * buf;
         const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
 #pragma unroll
         for (int kk = 0; kk < kHalf / 16; ++kk) {       // latent half: A = q_lat in TMEM
@@ -320,94 +343,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
     }
     __syncwarp();
-  } else if (warp < 6) {
-    // ---- sender warps 2..5: own partial scores -> the peer's receive buffer ----------
-    int* osh = reinterpret_cast<int*>(sm + OFF_OSH);
-    const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-    bool alive = true;
-    for (int j = 0; alive && j < nt; ++j) {
-      const int buf = j & 1;
-      alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
-      if (!alive) break;
-      tc_fence_after();
-      float sv[2][32];
-      tmem_ld32(tmem + lane_addr + kColSP + 64 * buf, sv[0]);
-      tmem_ld32(tmem + lane_addr + kColSP + 64 * buf + 32, sv[1]);
-      tmem_wait_ld();
-      // Quantise the partial scores once, to fp16 with an exact power-of-two
-      // scale per row; the same words go to the peer and, through the first 32
-      // columns of this score buffer, to our own softmax warps.
-      uint32_t w[32];
-      float amax = 0.f;
-#pragma unroll
-      for (int k = 0; k < 32; ++k) amax = fmaxf(amax, fmaxf(fabsf(sv[0][k]), fabsf(sv[1][k])));
-      const int sh = fp16_shift(amax);
-      const float sc = pow2f(sh);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          __half2 h2 = __floats2half2_rn(sv[hh][2 * k] * sc, sv[hh][2 * k + 1] * sc);
-          w[16 * hh + k] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-      tmem_st32u(tmem + lane_addr + kColSP + 64 * buf, w);
-      osh[buf * BM + r] = sh;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_OWN + buf));
-      // the peer has consumed what we sent into this receive buffer two tiles ago
-      if (j >= 2) {
-        alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK + buf), ((j >> 1) - 1) & 1, st, limit,
-                                             W_TX_OK));
+  } else if (warp == kWarpPV) {
+    // ---- P.V issuer: O_c += P . c_kv[:, 256c : 256c+256] ------------------------------
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
+      bool alive = true;
+      int p_armed = 1;                             // phases of B_P_RX armed so far
+      for (int j = 0; j < nt; ++j) {
+        const int stg = j % kStages;
+        alive = wait(BAR(B_P_FULL), j & 1, st, limit, W_P_FULL);
+        if (alive) alive = wait(BAR(B_P_RX), j & 1, st, limit, W_P_RX);
+        // already complete (Q.K^T of tile j read this stage); orders the TMA data
+        if (alive) alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
         if (!alive) break;
-      }
-      // Receive layout, chunk-major: 16-byte chunk m = 2c + h of row r at
-      // (m * BM + r) * 16 holds words {2c, 2c+1, 2c+8, 2c+9} (h = 0) or
-      // {2c+16, 2c+17, 2c+24, 2c+25} (h = 1), the words one .16x256b softmax
-      // thread (c = t % 4) needs; one warp store is a contiguous 512-byte
-      // block.  The rows' shifts follow the data.
-      const uint32_t rx_row = mapa(sbase + OFF_RX + buf * kRxStride + r * 16, peer);
-      const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL + buf), peer);
+        // arm the peer's P rows of tile j+1 before our commit lets the peer send them
+        if (j + 1 < nt) { mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes); ++p_armed; }
+        tc_fence_after();
+        const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
 #pragma unroll
-      for (int cq = 0; cq < 4; ++cq)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int w0 = 2 * cq + 16 * h;
-          st_async_v4u(rx_row + (2 * cq + h) * BM * 16, w[w0], w[w0 + 1], w[w0 + 8], w[w0 + 9],
-                       rxfull_remote);
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          // A = P (K-major, 128B rows); B = V = c_kv columns of this CTA,
+          // MN-major: 64-column chunks kKVChunk apart (LBO), 8-key groups 1 KiB apart (SBO).
+          uint64_t ad = smem_desc(sbase + OFF_P + kk * 32, 16, 1024);
+          uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
+          mma_bf16(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0));
         }
-      st_async_u32(mapa(sbase + OFF_RX + buf * kRxStride + kRxData + r * 4, peer), (uint32_t)sh,
-                   rxfull_remote);
+        mma_commit(BAR(B_KV_EMPTY + stg));
+        mma_commit_multicast(BAR(B_P_EMPTY), 0x3);   // both CTAs may overwrite P
+      }
+      if (alive) mma_commit(BAR(B_O_FULL));
+      // After an abort: let the peer's P rows of an armed, unconsumed phase land.
+      if (!alive && p_armed > 0) drain_wait(BAR(B_P_RX), (p_armed - 1) & 1, 200000ull);
+      mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
+      wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
     }
-  } else if (warp < kWarpPV) {
-    // ---- softmax warps 6..13 ------------------------------------------------------------
-    // Warp (q, g) owns tile rows 32q + 16g .. +15 (TMEM lane quadrant q).  In the
-    // .16x256b layout thread t holds rows ra = base + t/4 and rb = ra + 8, keys
-    // 16k + 4c .. 16k + 4c + 3 (c = t % 4, k = 0..3) of each 64-key tile, so the
-    // four threads of a row meet through two shuffles.
+    __syncwarp();
+  } else {
+    // ---- warps 2..9: quadrant q = warp % 4 (its TMEM lanes 32q .. 32q+31) -------------
     const int q = warp & 3;
-    const int g = (warp - 6) >> 2;
+    const bool is_softmax = warp >= 6;
     const int c = lane & 3;
-    const int ra = 32 * q + 16 * g + (lane >> 2), rb = ra + 8;
-    const uint32_t lane16 = static_cast<uint32_t>(32 * q + 16 * g) << 16;
+    // .16x256b slices: own rows (softmax) at 32q + 16 rank, peer rows (sender) at
+    // 32q + 16 (1 - rank); thread t holds rows base + t/4 and base + t/4 + 8.
+    const int own_base = 32 * q + 16 * (int)rank, peer_base = 32 * q + 16 * (int)peer;
+    const uint32_t lane_own = static_cast<uint32_t>(own_base) << 16;
+    const uint32_t lane_peer = static_cast<uint32_t>(peer_base) << 16;
     const uint32_t lane32 = static_cast<uint32_t>(32 * q) << 16;
-    const int nrows = a.N * a.H;
-    const bool va = rt * BM + ra < nrows, vb = rt * BM + rb < nrows;
-    const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
-    float* lsum = reinterpret_cast<float*>(sm + OFF_LSUM);
-    const int* osh = reinterpret_cast<const int*>(sm + OFF_OSH);
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
     bool alive = true;
 
     if (nt > 0) {
       grid_dep_wait();   // q_lat is written by the absorb kernel
-      // Q half of tile row 32q + lane, latent columns 128g .. 128g+127 of this
-      // CTA's half -> TMEM [kColQ + 64g, +64) as bf16 pairs (.32x32b layout).
+      // Q half of tile row 32q + lane -> TMEM [kColQ, +128) as bf16 pairs
+      // (.32x32b layout); the sender warp stores words 0..63, the softmax warp 64..127.
       const int rq = rt * BM + 32 * q + lane;
       const bool vq = rq < nrows;
+      const int g = is_softmax ? 1 : 0;
       const uint4* src = reinterpret_cast<const uint4*>(
           static_cast<const __nv_bfloat16*>(a.q_lat) + (req_row0 + (vq ? rq : 0)) * 512 +
           rank * kHalf + 128 * g);
@@ -427,79 +417,126 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       if (lane == 0) mbar_arrive(BAR(B_Q_READY));
     }
 
-    if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL))
-      alive = __all_sync(0xffffffffu, wait(BAR(B_STALL), 0, st, limit, W_STALL));
-
-    int consumed = 0;                            // exchange tiles received so far
-    for (int j = 0; alive && j < nt; ++j) {
-      const int buf = j & 1;
-      alive = __all_sync(0xffffffffu, wait(BAR(B_OWN + buf), (j >> 1) & 1, st, limit, W_OWN));
-      if (!alive) break;
-      tc_fence_after();
-      // own quantised partial scores (fp16 pairs, columns 0..31 of the score buffer)
-      uint32_t ow[16];
-      tmem_ld_16x256b_x4(tmem + lane16 + kColSP + 64 * buf, ow);
-      const float oia = pow2f(-osh[buf * BM + ra]), oib = pow2f(-osh[buf * BM + rb]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));   // QK^T of tile j+2 may overwrite
-
-      // + the peer's partial scores (its st.async filled rx[buf]).  Both products
-      // are exact (fp16 times a power of two), so own + peer rounds to the same
-      // float in both CTAs whichever is added first.
-      alive = __all_sync(0xffffffffu,
-                         wait<true>(BAR(B_RX_FULL + buf), (j >> 1) & 1, st, limit, W_RX_FULL));
-      if (!alive) break;
-      consumed = j + 1;
-      if (warp == 6 && lane == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
-      float sa[16], sb[16];
-      {
-        const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
-        int psa, psb;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(psa) : "r"(rxb + kRxData + ra * 4) : "memory");
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(psb) : "r"(rxb + kRxData + rb * 4) : "memory");
-        const float pia = pow2f(-psa), pib = pow2f(-psb);
+    if (!is_softmax) {
+      // ---- sender: the peer's score rows -> the peer's receive buffer ---------------
+      for (int j = 0; alive && j < nt; ++j) {
+        const int buf = j & 1;
+        alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
+        if (!alive) break;
+        tc_fence_after();
+        uint32_t v[32];
+        tmem_ld_16x256b_x8(tmem + lane_peer + kColS + 64 * buf, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));
+        // one power-of-two scale per row: the row's 64 values are spread over
+        // the 4 threads t with the same t / 4
+        float ma = 0.f, mb = 0.f;
 #pragma unroll
-        for (int rsel = 0; rsel < 2; ++rsel) {
-          const int row = rsel ? rb : ra;
-          const float pinv = rsel ? pib : pia, oinv = rsel ? oib : oia;
-          float* sv = rsel ? sb : sa;
-          uint32_t pw[8];
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(pw[4 * h]), "=r"(pw[4 * h + 1]), "=r"(pw[4 * h + 2]),
-                           "=r"(pw[4 * h + 3])
-                         : "r"(rxb + ((2 * c + h) * BM + row) * 16) : "memory");
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              // key 16k + 4c + 2e (+1): own word ow[4k + 2 rsel + e], peer word pw[2k + e]
-              const float2 fo = __half22float2(*reinterpret_cast<const __half2*>(&ow[4 * k + 2 * rsel + e]));
-              const float2 fp = __half22float2(*reinterpret_cast<const __half2*>(&pw[2 * k + e]));
-              sv[4 * k + 2 * e] = fmaf(fp.x, pinv, fo.x * oinv);
-              sv[4 * k + 2 * e + 1] = fmaf(fp.y, pinv, fo.y * oinv);
-            }
+        for (int k = 0; k < 8; ++k) {
+          ma = max3f(ma, fabsf(__uint_as_float(v[4 * k])), fabsf(__uint_as_float(v[4 * k + 1])));
+          mb = max3f(mb, fabsf(__uint_as_float(v[4 * k + 2])), fabsf(__uint_as_float(v[4 * k + 3])));
         }
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+        const int sha = fp16_shift(ma), shb = fp16_shift(mb);
+        const float sca = pow2f(sha), scb = pow2f(shb);
+        uint32_t w[16];                            // rows a then b, key pairs 8k + 2c
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          __half2 ha = __floats2half2_rn(__uint_as_float(v[4 * k]) * sca,
+                                         __uint_as_float(v[4 * k + 1]) * sca);
+          __half2 hb = __floats2half2_rn(__uint_as_float(v[4 * k + 2]) * scb,
+                                         __uint_as_float(v[4 * k + 3]) * scb);
+          w[k] = *reinterpret_cast<uint32_t*>(&ha);
+          w[8 + k] = *reinterpret_cast<uint32_t*>(&hb);
+        }
+        // the peer has consumed what we sent into this receive buffer two tiles ago
+        if (j >= 2) {
+          alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK + buf), ((j >> 1) - 1) & 1, st, limit,
+                                               W_TX_OK));
+          if (!alive) break;
+        }
+        const uint32_t rxp = mapa(sbase + OFF_RX + buf * kRxStride, peer);
+        const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL + buf), peer);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          st_async_v4u(rxp + ((q * 4 + m) * 32 + lane) * 16, w[4 * m], w[4 * m + 1], w[4 * m + 2],
+                       w[4 * m + 3], rxfull_remote);
+        st_async_u32(rxp + kRxData + (q * 32 + lane) * 4,
+                     ((uint32_t)sha & 0xffffu) | ((uint32_t)shb << 16), rxfull_remote);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));  // consumed
+    } else {
+      // ---- softmax of this CTA's rows ra = own_base + t/4, rb = ra + 8 ---------------
+      // Thread t holds keys 8k + 2c, 8k + 2c + 1 (k = 0..7) of each 64-key tile.
+      const int ra = own_base + (lane >> 2), rb = ra + 8;
+      const bool va = rt * BM + ra < nrows, vb = rt * BM + rb < nrows;
+      const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
+      const float* af = reinterpret_cast<const float*>(sm + OFF_AF);
+      float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
 
-      // visibility mask (only tiles that reach past the prefix, or rows past the end)
-      const int tb = k0 + j * BN;
-      if (!(va && vb && tb + BN <= L)) {
+      if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL))
+        alive = __all_sync(0xffffffffu, wait(BAR(B_STALL), 0, st, limit, W_STALL));
+
+      int consumed = 0, af_consumed = 0;          // exchange tiles received so far
+      for (int j = 0; alive && j < nt; ++j) {
+        const int buf = j & 1;
+        alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
+        if (!alive) break;
+        tc_fence_after();
+        uint32_t v[32];                            // own partial scores (fp32)
+        tmem_ld_16x256b_x8(tmem + lane_own + kColS + 64 * buf, v);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));   // QK^T of tile j+2 may overwrite
+
+        // + the peer's partial scores for our rows (its st.async filled rx[buf])
+        alive = __all_sync(0xffffffffu,
+                           wait<true>(BAR(B_RX_FULL + buf), (j >> 1) & 1, st, limit, W_RX_FULL));
+        if (!alive) break;
+        consumed = j + 1;
+        if (warp == 6 && lane == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
+        float sa[16], sb[16];
+        {
+          const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
+          uint32_t pw[16], shw;
 #pragma unroll
-        for (int rsel = 0; rsel < 2; ++rsel) {
-          const bool vrow = rsel ? vb : va;
-          const int node = vrow ? (rt * BM + (rsel ? rb : ra)) / a.H : 0;
-          float* sv = rsel ? sb : sa;
+          for (int m = 0; m < 4; ++m)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(pw[4 * m]), "=r"(pw[4 * m + 1]), "=r"(pw[4 * m + 2]), "=r"(pw[4 * m + 3])
+                         : "r"(rxb + ((q * 4 + m) * 32 + lane) * 16) : "memory");
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(shw) : "r"(rxb + kRxData + (q * 32 + lane) * 4)
+                       : "memory");
+          const float pia = pow2f(-(int)(int16_t)(shw & 0xffffu));
+          const float pib = pow2f(-(int)(int16_t)(shw >> 16));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < 8; ++k) {
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pw[k]));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pw[8 + k]));
+            sa[2 * k] = fmaf(fa.x, pia, __uint_as_float(v[4 * k]));
+            sa[2 * k + 1] = fmaf(fa.y, pia, __uint_as_float(v[4 * k + 1]));
+            sb[2 * k] = fmaf(fb.x, pib, __uint_as_float(v[4 * k + 2]));
+            sb[2 * k + 1] = fmaf(fb.y, pib, __uint_as_float(v[4 * k + 3]));
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));  // consumed
+
+        // visibility mask (only tiles that reach past the prefix, or rows past the end)
+        const int tb = k0 + j * BN;
+        if (!(va && vb && tb + BN <= L)) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int t = tb + 16 * k + 4 * c + e;
+          for (int rsel = 0; rsel < 2; ++rsel) {
+            const bool vrow = rsel ? vb : va;
+            const int node = vrow ? (rt * BM + (rsel ? rb : ra)) / a.H : 0;
+            float* sv = rsel ? sb : sa;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int t = tb + 8 * (i >> 1) + 2 * c + (i & 1);
               bool vis = false;
               if (vrow && t < k1) {
                 if (t < L) {
@@ -509,149 +546,146 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                   vis = (anc[4 * node + (jn >> 5)] >> (jn & 31)) & 1u;
                 }
               }
-              if (!vis) sv[4 * k + e] = -INFINITY;
+              if (!vis) sv[i] = -INFINITY;
             }
+          }
         }
-      }
-      // row maxima: 16 keys per thread, then the row's four threads
-      float mta = sa[0], mtb = sb[0];
+        // row maxima: 16 keys per thread, then the row's four threads
+        float mta = max3f(sa[0], sa[1], sa[2]), mtb = max3f(sb[0], sb[1], sb[2]);
 #pragma unroll
-      for (int k = 1; k < 16; ++k) { mta = fmaxf(mta, sa[k]); mtb = fmaxf(mtb, sb[k]); }
-      mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 1));
-      mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 1));
-      mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 2)) * sl2;
-      mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 2)) * sl2;
+        for (int k = 3; k < 15; k += 2) {
+          mta = max3f(mta, sa[k], sa[k + 1]);
+          mtb = max3f(mtb, sb[k], sb[k + 1]);
+        }
+        mta = fmaxf(mta, sa[15]);
+        mtb = fmaxf(mtb, sb[15]);
+        mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 1));
+        mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 1));
+        mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 2)) * sl2;
+        mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 2)) * sl2;
 
-      // lazy rescale: move the reference max only when it grows by > 8 (log2);
-      // the four threads of a row take the same decision from the same inputs
-      float alpha_a = 1.f, alpha_b = 1.f;
-      bool rescale = false;
-      if (mta > m_a + 8.f) {
-        if (m_a != -INFINITY) { alpha_a = ex2(m_a - mta); rescale = true; }
-        l_a *= alpha_a;
-        m_a = mta;
-      }
-      if (mtb > m_b + 8.f) {
-        if (m_b != -INFINITY) { alpha_b = ex2(m_b - mtb); rescale = true; }
-        l_b *= alpha_b;
-        m_b = mtb;
-      }
-      const float nma = m_a == -INFINITY ? 0.f : -m_a, nmb = m_b == -INFINITY ? 0.f : -m_b;
-      uint32_t pk[16];                            // [row][k][pair]: bf16 pairs of P
-      float psa = 0.f, psb = 0.f;
+        // lazy rescale: move the reference max only when it grows by > 8 (log2)
+        float alpha_a = 1.f, alpha_b = 1.f;
+        if (mta > m_a + 8.f) {
+          if (m_a != -INFINITY) alpha_a = ex2(m_a - mta);
+          l_a *= alpha_a;
+          m_a = mta;
+        }
+        if (mtb > m_b + 8.f) {
+          if (m_b != -INFINITY) alpha_b = ex2(m_b - mtb);
+          l_b *= alpha_b;
+          m_b = mtb;
+        }
+        // our rows' rescale factors -> the peer (it rescales its half of O)
+        {
+          const int afb = j & (kAfBufs - 1);
+          const uint32_t afr = mapa(BAR(B_AF_FULL + afb), peer);
+          if (c < 2)
+            st_async_u32(mapa(sbase + OFF_AF + (afb * BM + (c ? rb : ra)) * 4, peer),
+                         __float_as_uint(c ? alpha_b : alpha_a), afr);
+        }
+        const float nma = m_a == -INFINITY ? 0.f : -m_a, nmb = m_b == -INFINITY ? 0.f : -m_b;
+        uint32_t pa[8], pb[8];                     // bf16 pairs of P: keys 8k + 2c, +1
+        float psa = 0.f, psb = 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t ha = pack_bf16x2(ex2(fmaf(sa[2 * k], sl2, nma)), ex2(fmaf(sa[2 * k + 1], sl2, nma)));
-        const uint32_t hb = pack_bf16x2(ex2(fmaf(sb[2 * k], sl2, nmb)), ex2(fmaf(sb[2 * k + 1], sl2, nmb)));
-        pk[k] = ha;
-        pk[8 + k] = hb;
-        psa += __uint_as_float(ha << 16) + __uint_as_float(ha & 0xffff0000u);
-        psb += __uint_as_float(hb << 16) + __uint_as_float(hb & 0xffff0000u);
-      }
-      l_a += psa;
-      l_b += psb;
+        for (int k = 0; k < 8; ++k) {
+          pa[k] = pack_bf16x2(ex2(fmaf(sa[2 * k], sl2, nma)), ex2(fmaf(sa[2 * k + 1], sl2, nma)));
+          pb[k] = pack_bf16x2(ex2(fmaf(sb[2 * k], sl2, nmb)), ex2(fmaf(sb[2 * k + 1], sl2, nmb)));
+          psa += __uint_as_float(pa[k] << 16) + __uint_as_float(pa[k] & 0xffff0000u);
+          psb += __uint_as_float(pb[k] << 16) + __uint_as_float(pb[k] & 0xffff0000u);
+        }
+        l_a += psa;
+        l_b += psb;
 
-      // the P buffer is free once P.V of tile j-2 (same buffer) has completed;
-      // O is stable once P.V of tile j-1 has completed
-      if (j >= 2) {
+        // the peer's rescale factors for its rows of this quadrant
+        const int afb = j & (kAfBufs - 1);
         alive = __all_sync(0xffffffffu,
-                           wait(BAR(B_P_EMPTY + buf), ((j >> 1) - 1) & 1, st, limit, W_P_EMPTY));
+                           wait<true>(BAR(B_AF_FULL + afb), (j / kAfBufs) & 1, st, limit, W_AF));
         if (!alive) break;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
+        af_consumed = j + 1;
+        const float qa = af[afb * BM + (ra ^ 16)], qb = af[afb * BM + (rb ^ 16)];
+        if (warp == 6 && lane == 0 && j + kAfBufs < nt)
+          mbar_expect_tx(BAR(B_AF_FULL + afb), kAfBytes);
+
+        // P (single buffer) is free, and O stable, once P.V of tile j-1 completed in both CTAs
         if (j >= 1) {
-          alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + (buf ^ 1)), ((j - 1) >> 1) & 1, st,
-                                               limit, W_P_EMPTY));
+          alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY), (j - 1) & 1, st, limit, W_P_EMPTY));
           if (!alive) break;
         }
-        tc_fence_after();
-        for (int cc = 0; cc < kHalf / 64; ++cc) {     // this warp's 16 rows x 256 O columns
-          uint32_t ov[32];
-          const uint32_t oa = tmem + lane16 + kColO + 64 * cc;
-          tmem_ld_16x256b_x8(oa, ov);
-          tmem_wait_ld();
+        if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f || qa != 1.f || qb != 1.f)) {
+          tc_fence_after();
+          rescale_o_rows(tmem + lane_own + kColO, alpha_a, alpha_b);
+          rescale_o_rows(tmem + lane_peer + kColO, qa, qb);
+          tmem_wait_st();
+          tc_fence_before();
+        }
+        // P rows ra, rb: the pair for keys 8k + 2c is 4 bytes at offset 4c of the
+        // row's 16-byte chunk k, stored 128B-swizzled (chunk k of row r at k ^ (r & 7)).
+        {
+          const uint32_t prow_a = sbase + OFF_P + ra * 128 + 4 * c;
+          const uint32_t prow_b = sbase + OFF_P + rb * 128 + 4 * c;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            ov[4 * k] = __float_as_uint(__uint_as_float(ov[4 * k]) * alpha_a);
-            ov[4 * k + 1] = __float_as_uint(__uint_as_float(ov[4 * k + 1]) * alpha_a);
-            ov[4 * k + 2] = __float_as_uint(__uint_as_float(ov[4 * k + 2]) * alpha_b);
-            ov[4 * k + 3] = __float_as_uint(__uint_as_float(ov[4 * k + 3]) * alpha_b);
+            asm volatile("st.shared.b32 [%0], %1;" :: "r"(prow_a + ((k ^ (ra & 7)) << 4)), "r"(pa[k]) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" :: "r"(prow_b + ((k ^ (rb & 7)) << 4)), "r"(pb[k]) : "memory");
           }
-          tmem_st_16x256b_x8(oa, ov);
         }
-        tmem_wait_st();
-        tc_fence_before();
+        fence_async_smem();                         // visible to the tensor core and the copy engine
+        __syncwarp();
+        if (lane == 0) {
+          // our 16 rows of this quadrant are one contiguous 2 KiB block
+          const uint32_t off = OFF_P + own_base * 128;
+          bulk_copy_to_peer(mapa(sbase + off, peer), sbase + off, kPQuadBytes,
+                            mapa(BAR(B_P_RX), peer));
+          mbar_arrive(BAR(B_P_FULL));
+        }
       }
-      // P rows ra, rb: keys 16k + 4c .. +3 are 8 bytes at offset 8(c & 1) of the
-      // row's 16-byte chunk 2k + c/2, stored 128B-swizzled (chunk m of row r at
-      // m ^ (r & 7)): the K-major A operand layout of P.V.
-      {
-        const uint32_t pb = sbase + OFF_P + buf * kPBytes;
+
+      // After an abort, let what the peer may still be sending land before exit
+      // (receive phases that were armed but not consumed); bounded, errors ignored.
+      for (int t = consumed; t < consumed + 2 && t < nt; ++t)
+        drain_wait(BAR(B_RX_FULL + (t & 1)), (t >> 1) & 1, 200000ull);
+      for (int t = af_consumed; t < af_consumed + kAfBufs && t < nt; ++t)
+        drain_wait(BAR(B_AF_FULL + (t & (kAfBufs - 1))), (t / kAfBufs) & 1, 200000ull);
+
+      // (m, l) of our rows: row sums meet across the row's four threads
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+      if (ok && alive && c == 0) {
+        const long long rows = (long long)a.B * a.N * a.H;
 #pragma unroll
         for (int rsel = 0; rsel < 2; ++rsel) {
-          const int row = rsel ? rb : ra;
-          const uint32_t prow = pb + (row >> 3) * 1024 + (row & 7) * 128 + 8 * (c & 1);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            asm volatile("st.shared.v2.b32 [%0], {%1, %2};"
-                         :: "r"(prow + (((2 * k + (c >> 1)) ^ (row & 7)) << 4)),
-                            "r"(pk[8 * rsel + 2 * k]), "r"(pk[8 * rsel + 2 * k + 1]) : "memory");
+          const bool vrow = rsel ? vb : va;
+          const float l = rsel ? l_b : l_a, m = rsel ? m_b : m_a;
+          if (vrow) {
+            float* ml = a.part_ml + ((long long)s * rows + req_row0 + rt * BM + (rsel ? rb : ra)) * 2;
+            const bool has = nt > 0 && l > 0.f;
+            ml[0] = has ? m * 0.6931471805599453f : -INFINITY;
+            ml[1] = has ? l : 0.f;
+          }
         }
       }
-      fence_async_smem();                         // visible to the tensor core
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_P_FULL + buf));
     }
 
-    // After an abort, let score rows the peer may still be sending land before exit
-    // (receive phases that were armed but not consumed); bounded, errors ignored.
-    for (int t = consumed; t < consumed + 2 && t < nt; ++t)
-      drain_wait(BAR(B_RX_FULL + (t & 1)), (t >> 1) & 1, 200000ull);
-
-    // ---- epilogue: unnormalised partial o_lat half, (m, l) -----------------------------
-    // Row sums meet across the row's four threads; the (m, l) of every row go
-    // through shared memory to the .32x32b read-out below (thread = row
-    // 32q + lane, O columns 128g .. 128g+127).
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    // ---- epilogue: unnormalised partial o_lat half of rows 32q .. 32q+31 ----------------
+    // (.32x32b: thread = row; the sender warp writes O columns 0..127, the softmax 128..255)
     if (alive && nt > 0)
       alive = __all_sync(0xffffffffu, wait(BAR(B_O_FULL), 0, st, limit, W_O_FULL));
-    float l_sum = 0.f, m_row = -INFINITY;
-    const int r = 32 * q + lane;                 // read-out row
+    const int r = 32 * q + lane;
     const int rr = rt * BM + r;
-    const bool row_valid = rr < nrows;
-    if (alive && nt > 0) {
-      if (c == 0) {
-        lsum[ra] = l_a; lsum[BM + ra] = m_a;
-        lsum[rb] = l_b; lsum[BM + rb] = m_b;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_LSUM));
-      alive = __all_sync(0xffffffffu, wait(BAR(B_LSUM), 0, st, limit, W_O_FULL));
-      if (alive) { l_sum = lsum[r]; m_row = lsum[BM + r]; }
-    }
-    // tcgen05.ld is warp-collective: every lane loads, only valid rows store.
-    const bool has_data = ok && alive && nt > 0 && row_valid && l_sum > 0.f;
-    if (ok && alive && row_valid && g == 0) {
+    if (ok && alive && nt > 0) {
       const long long rows = (long long)a.B * a.N * a.H;
-      float* ml = a.part_ml + ((long long)s * rows + req_row0 + rr) * 2;
-      if (rank == 0) {
-        ml[0] = has_data ? m_row * 0.6931471805599453f : -INFINITY;
-        ml[1] = has_data ? l_sum : 0.f;
-      }
-    }
-    if (ok && alive && nt > 0 && __any_sync(0xffffffffu, has_data)) {
-      const long long rows = (long long)a.B * a.N * a.H;
-      float* po = a.part_o + ((long long)s * rows + req_row0 + (has_data ? rr : 0)) * a.d_c +
+      const int g = is_softmax ? 1 : 0;
+      float* po = a.part_o + ((long long)s * rows + req_row0 + (rr < nrows ? rr : 0)) * a.d_c +
                   rank * kHalf + 128 * g;
       tc_fence_after();
       for (int cc = 0; cc < 4; ++cc) {
         float ov[32];
         tmem_ld32(tmem + lane32 + kColO + 128 * g + 32 * cc, ov);
         tmem_wait_ld();
-        if (has_data) {
+        if (rr < nrows) {
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
             *reinterpret_cast<float4*>(po + 32 * cc + k) =
@@ -659,36 +693,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         }
       }
     }
-  } else {
-    // ---- P.V issuer (warp 14): O_c += P . c_kv[:, 256c : 256c+256] -------------------
-    if (lane == 0 && nt > 0) {
-      constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
-      bool alive = true;
-      for (int j = 0; j < nt; ++j) {
-        const int stg = j % kStages, buf = j & 1;
-        alive = wait(BAR(B_P_FULL + buf), (j >> 1) & 1, st, limit, W_P_FULL);
-        // already complete (Q.K^T of tile j read this stage); orders the TMA data
-        if (alive) alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
-        if (!alive) break;
-        tc_fence_after();
-        const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
-        const uint32_t pb = sbase + OFF_P + buf * kPBytes;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P (K-major, 128B rows); B = V = c_kv columns of this CTA,
-          // MN-major: 64-column chunks kKVChunk apart (LBO), 8-key groups 1 KiB apart (SBO).
-          uint64_t ad = smem_desc(pb + kk * 32, 16, 1024);
-          uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
-          mma_bf16(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0));
-        }
-        mma_commit(BAR(B_KV_EMPTY + stg));
-        mma_commit(BAR(B_P_EMPTY + buf));
-      }
-      if (alive) mma_commit(BAR(B_O_FULL));
-      mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
-      wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
-    }
-    __syncwarp();
   }
 
   // ---- teardown ------------------------------------------------------------------------
