@@ -597,27 +597,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         l_a += psa;
         l_b += psb;
 
-        // the peer's rescale factors for its rows of this quadrant
-        const int afb = j & (kAfBufs - 1);
-        alive = __all_sync(0xffffffffu,
-                           wait<true>(BAR(B_AF_FULL + afb), (j / kAfBufs) & 1, st, limit, W_AF));
-        if (!alive) break;
-        af_consumed = j + 1;
-        const float qa = af[afb * BM + (ra ^ 16)], qb = af[afb * BM + (rb ^ 16)];
-        if (warp == 6 && lane == 0 && j + kAfBufs < nt)
-          mbar_expect_tx(BAR(B_AF_FULL + afb), kAfBytes);
-
         // P (single buffer) is free, and O stable, once P.V of tile j-1 completed in both CTAs
         if (j >= 1) {
           alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY), (j - 1) & 1, st, limit, W_P_EMPTY));
           if (!alive) break;
-        }
-        if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f || qa != 1.f || qb != 1.f)) {
-          tc_fence_after();
-          rescale_o_rows(tmem + lane_own + kColO, alpha_a, alpha_b);
-          rescale_o_rows(tmem + lane_peer + kColO, qa, qb);
-          tmem_wait_st();
-          tc_fence_before();
         }
         // P rows ra, rb: the pair for keys 8k + 2c is 4 bytes at offset 4c of the
         // row's 16-byte chunk k, stored 128B-swizzled (chunk k of row r at k ^ (r & 7)).
@@ -637,8 +620,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           const uint32_t off = OFF_P + own_base * 128;
           bulk_copy_to_peer(mapa(sbase + off, peer), sbase + off, kPQuadBytes,
                             mapa(BAR(B_P_RX), peer));
-          mbar_arrive(BAR(B_P_FULL));
         }
+        // the peer's rescale factors for its rows of this quadrant: both halves of
+        // O must carry the same reference maxima before P.V of this tile
+        const int afb = j & (kAfBufs - 1);
+        alive = __all_sync(0xffffffffu,
+                           wait<true>(BAR(B_AF_FULL + afb), (j / kAfBufs) & 1, st, limit, W_AF));
+        if (!alive) break;
+        af_consumed = j + 1;
+        const float qa = af[afb * BM + (ra ^ 16)], qb = af[afb * BM + (rb ^ 16)];
+        if (warp == 6 && lane == 0 && j + kAfBufs < nt)
+          mbar_expect_tx(BAR(B_AF_FULL + afb), kAfBytes);
+        if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f || qa != 1.f || qb != 1.f)) {
+          tc_fence_after();
+          rescale_o_rows(tmem + lane_own + kColO, alpha_a, alpha_b);
+          rescale_o_rows(tmem + lane_peer + kColO, qa, qb);
+          tmem_wait_st();
+          tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_P_FULL));
       }
 
       // After an abort, let what the peer may still be sending land before exit
