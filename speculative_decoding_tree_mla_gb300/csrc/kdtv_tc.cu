@@ -77,8 +77,8 @@ constexpr int kRxBytes = kRxData + 4 * 32 * 4;
 constexpr int kRxStride = (kRxBytes + 127) / 128 * 128;
 constexpr int kAfBufs = 4;              // rescale-factor buffers, [BM] floats each
 constexpr int kAfBytes = 64 * 4;        // the peer's 64 rows per tile
-constexpr int kThreads = 352;
-constexpr int kWarpPV = 10;
+constexpr int kThreads = 480;
+constexpr int kWarpPV = 14;
 constexpr int kTmemCols = 512;
 constexpr int kColO = 0;
 constexpr int kColQ = 256;
@@ -91,8 +91,10 @@ constexpr int OFF_RX = OFF_P + kPBytes;                        // two receive bu
 constexpr int OFF_AF = OFF_RX + 2 * kRxStride;                 // [kAfBufs][BM] floats
 constexpr int OFF_ANC = OFF_AF + kAfBufs * BM * 4;
 constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 16;              // staged parent[]
-constexpr int OFF_BAR = OFF_PAR + kMaxNodes * 4;
-constexpr int kNumBars = 32;
+constexpr int OFF_MREF = OFF_PAR + kMaxNodes * 4;              // [2 parities][BM] reference maxima
+constexpr int OFF_LPART = OFF_MREF + 2 * BM * 4;                // [m | l][BM] of the odd-tile warps
+constexpr int OFF_BAR = OFF_LPART + 2 * BM * 4;
+constexpr int kNumBars = 40;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -113,17 +115,19 @@ enum Bar : int {
   B_AF_FULL = B_TX_OK + 2,           // [kAfBufs] the peer's rescale factors landed (tx)
   B_P_FULL = B_AF_FULL + kAfBufs,    // our softmax wrote its P rows
   B_P_RX = B_P_FULL + 1,             // the peer's P rows landed (tx)
-  B_P_EMPTY = B_P_RX + 1,            // P.V of the tile completed in both CTAs
-  B_O_FULL = B_P_EMPTY + 1,
+  B_P_EMPTY = B_P_RX + 1,            // [2] P.V of an even / odd tile completed in both CTAs
+  B_O_FULL = B_P_EMPTY + 2,
   B_MMA_DONE = B_O_FULL + 1,         // both MMA issuers drained
   B_STALL = B_MMA_DONE + 1,
-  B_COUNT = B_STALL + 1
+  B_MREF = B_STALL + 1,              // [2 parities][4 quadrants] reference maxima published
+  B_LSUM = B_MREF + 8,               // the odd-tile softmax warps published their (m, l)
+  B_COUNT = B_LSUM + 1
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 
 // Wait sites (reported as the timeout detail).
 enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK, W_RX_FULL,
-            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_AF, W_P_RX };
+            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_AF, W_P_RX, W_MREF, W_LSUM };
 
 struct TcCfg {
   int row_tiles;               // ceil(N * H / 128)
@@ -209,10 +213,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     for (int i = 0; i < kAfBufs; ++i) mbar_init(BAR(B_AF_FULL + i), 1);
     mbar_init(BAR(B_P_FULL), 4);          // our 4 softmax warps
     mbar_init(BAR(B_P_RX), 1);            // armed with expect_tx; filled by the peer's bulk copies
-    mbar_init(BAR(B_P_EMPTY), 2);         // P.V commits of both CTAs (multicast)
+    // P.V commits of both CTAs (multicast), one barrier per tile parity: each
+    // softmax warp waits only for the other parity's tiles, so it sees every
+    // phase of the barrier it waits on in order.
+    mbar_init(BAR(B_P_EMPTY + 0), 2);
+    mbar_init(BAR(B_P_EMPTY + 1), 2);
     mbar_init(BAR(B_O_FULL), 1);
     mbar_init(BAR(B_MMA_DONE), 2);
     mbar_init(BAR(B_STALL), 1);
+    for (int i = 0; i < 8; ++i) mbar_init(BAR(B_MREF + i), 1);
+    mbar_init(BAR(B_LSUM), 4);
     mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchanges of tiles 0 and 1
     mbar_expect_tx(BAR(B_RX_FULL + 1), kRxBytes);
     for (int i = 0; i < kAfBufs; ++i) mbar_expect_tx(BAR(B_AF_FULL + i), kAfBytes);
@@ -369,7 +379,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           mma_bf16(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0));
         }
         mma_commit(BAR(B_KV_EMPTY + stg));
-        mma_commit_multicast(BAR(B_P_EMPTY), 0x3);   // both CTAs may overwrite P
+        mma_commit_multicast(BAR(B_P_EMPTY + (j & 1)), 0x3);   // both CTAs may overwrite P
       }
       if (alive) mma_commit(BAR(B_O_FULL));
       // After an abort: let the peer's P rows of an armed, unconsumed phase land.
@@ -379,9 +389,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     }
     __syncwarp();
   } else {
-    // ---- warps 2..9: quadrant q = warp % 4 (its TMEM lanes 32q .. 32q+31) -------------
+    // ---- warps 2..13: quadrant q = warp % 4 (its TMEM lanes 32q .. 32q+31) ------------
     const int q = warp & 3;
     const bool is_softmax = warp >= 6;
+    const int par = is_softmax ? (warp - 6) >> 2 : 0;   // softmax: even (0) or odd (1) tiles
     const int c = lane & 3;
     // .16x256b slices: own rows (softmax) at 32q + 16 rank, peer rows (sender) at
     // 32q + 16 (1 - rank); thread t holds rows base + t/4 and base + t/4 + 8.
@@ -391,10 +402,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     const uint32_t lane32 = static_cast<uint32_t>(32 * q) << 16;
     bool alive = true;
 
-    if (nt > 0) {
+    if (nt > 0 && par == 0) {
       grid_dep_wait();   // q_lat is written by the absorb kernel
       // Q half of tile row 32q + lane -> TMEM [kColQ, +128) as bf16 pairs
-      // (.32x32b layout); the sender warp stores words 0..63, the softmax warp 64..127.
+      // (.32x32b layout); the sender warp stores words 0..63, the even-tile softmax
+      // warp 64..127.
       const int rq = rt * BM + 32 * q + lane;
       const bool vq = rq < nrows;
       const int g = is_softmax ? 1 : 0;
@@ -476,13 +488,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       const bool va = rt * BM + ra < nrows, vb = rt * BM + rb < nrows;
       const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
       const float* af = reinterpret_cast<const float*>(sm + OFF_AF);
+      float* mref = reinterpret_cast<float*>(sm + OFF_MREF);
+      float* lpart = reinterpret_cast<float*>(sm + OFF_LPART);
+      // Reference maxima last used by this warp and its row sums relative to them.
       float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+      const int lead = 6 + 4 * par;               // the warp that re-arms this parity's receive barriers
 
       if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL))
         alive = __all_sync(0xffffffffu, wait(BAR(B_STALL), 0, st, limit, W_STALL));
 
-      int consumed = 0, af_consumed = 0;          // exchange tiles received so far
-      for (int j = 0; alive && j < nt; ++j) {
+      // This warp takes the tiles j = par, par + 2, ...; the running reference
+      // maxima pass between the two warps of the quadrant through shared memory.
+      int next_rx = par;                          // first receive phase not yet consumed
+      int next_af = par;
+      for (int j = par; alive && j < nt; j += 2) {
         const int buf = j & 1;
         alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
         if (!alive) break;
@@ -498,8 +517,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         alive = __all_sync(0xffffffffu,
                            wait<true>(BAR(B_RX_FULL + buf), (j >> 1) & 1, st, limit, W_RX_FULL));
         if (!alive) break;
-        consumed = j + 1;
-        if (warp == 6 && lane == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
+        next_rx = j + 2;
+        if (warp == lead && lane == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
         float sa[16], sb[16];
         {
           const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
@@ -564,17 +583,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 2)) * sl2;
         mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 2)) * sl2;
 
-        // lazy rescale: move the reference max only when it grows by > 8 (log2)
-        float alpha_a = 1.f, alpha_b = 1.f;
-        if (mta > m_a + 8.f) {
-          if (m_a != -INFINITY) alpha_a = ex2(m_a - mta);
-          l_a *= alpha_a;
-          m_a = mta;
+        // the reference maxima after tile j-1 (the other warp of this quadrant)
+        float mpa = -INFINITY, mpb = -INFINITY;
+        if (j >= 1) {
+          alive = __all_sync(0xffffffffu, wait(BAR(B_MREF + 4 * (par ^ 1) + q), ((j - 1) >> 1) & 1,
+                                               st, limit, W_MREF));
+          if (!alive) break;
+          mpa = mref[(par ^ 1) * BM + ra];
+          mpb = mref[(par ^ 1) * BM + rb];
         }
-        if (mtb > m_b + 8.f) {
-          if (m_b != -INFINITY) alpha_b = ex2(m_b - mtb);
-          l_b *= alpha_b;
-          m_b = mtb;
+        // lazy rescale: move the reference max only when it grows by > 8 (log2);
+        // alpha rescales O (all tiles so far) to the new reference
+        float alpha_a = 1.f, alpha_b = 1.f;
+        float mna = mpa, mnb = mpb;
+        if (mta > mpa + 8.f) {
+          if (mpa != -INFINITY) alpha_a = ex2(mpa - mta);
+          mna = mta;
+        }
+        if (mtb > mpb + 8.f) {
+          if (mpb != -INFINITY) alpha_b = ex2(mpb - mtb);
+          mnb = mtb;
+        }
+        if (c == 0) {
+          mref[par * BM + ra] = mna;
+          mref[par * BM + rb] = mnb;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_MREF + 4 * par + q));
+        // this warp's row sums follow the reference
+        if (mna != m_a) {
+          if (m_a != -INFINITY) l_a *= ex2(m_a - mna);
+          m_a = mna;
+        }
+        if (mnb != m_b) {
+          if (m_b != -INFINITY) l_b *= ex2(m_b - mnb);
+          m_b = mnb;
         }
         // our rows' rescale factors -> the peer (it rescales its half of O)
         {
@@ -597,9 +640,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         l_a += psa;
         l_b += psb;
 
-        // P (single buffer) is free, and O stable, once P.V of tile j-1 completed in both CTAs
+        // P (single buffer) is free, and O stable, once P.V of tile j-1 completed in
+        // both CTAs (the (j-1)/2-th phase of the other parity's barrier)
         if (j >= 1) {
-          alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY), (j - 1) & 1, st, limit, W_P_EMPTY));
+          alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, st,
+                                               limit, W_P_EMPTY));
           if (!alive) break;
         }
         // P rows ra, rb: the pair for keys 8k + 2c is 4 bytes at offset 4c of the
@@ -627,9 +672,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         alive = __all_sync(0xffffffffu,
                            wait<true>(BAR(B_AF_FULL + afb), (j / kAfBufs) & 1, st, limit, W_AF));
         if (!alive) break;
-        af_consumed = j + 1;
+        next_af = j + 2;
         const float qa = af[afb * BM + (ra ^ 16)], qb = af[afb * BM + (rb ^ 16)];
-        if (warp == 6 && lane == 0 && j + kAfBufs < nt)
+        if (warp == lead && lane == 0 && j + kAfBufs < nt)
           mbar_expect_tx(BAR(B_AF_FULL + afb), kAfBytes);
         if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f || qa != 1.f || qb != 1.f)) {
           tc_fence_after();
@@ -644,17 +689,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
 
       // After an abort, let what the peer may still be sending land before exit
       // (receive phases that were armed but not consumed); bounded, errors ignored.
-      for (int t = consumed; t < consumed + 2 && t < nt; ++t)
-        drain_wait(BAR(B_RX_FULL + (t & 1)), (t >> 1) & 1, 200000ull);
-      for (int t = af_consumed; t < af_consumed + kAfBufs && t < nt; ++t)
-        drain_wait(BAR(B_AF_FULL + (t & (kAfBufs - 1))), (t / kAfBufs) & 1, 200000ull);
+      if (!alive) {
+        if (next_rx < nt) drain_wait(BAR(B_RX_FULL + (next_rx & 1)), (next_rx >> 1) & 1, 200000ull);
+        for (int t = next_af; t < next_af + kAfBufs && t < nt; t += 2)
+          drain_wait(BAR(B_AF_FULL + (t & (kAfBufs - 1))), (t / kAfBufs) & 1, 200000ull);
+      }
 
       // (m, l) of our rows: row sums meet across the row's four threads
       l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
       l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
       l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-      if (ok && alive && c == 0) {
+      // the odd-tile warp hands its (m, l) to the even-tile warp, which merges
+      // them (the later reference is the larger) and writes the row's (m, l)
+      if (par == 1) {
+        if (c == 0) {
+          lpart[ra] = m_a; lpart[BM + ra] = l_a;
+          lpart[rb] = m_b; lpart[BM + rb] = l_b;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_LSUM));
+      } else if (ok) {
+        alive = __all_sync(0xffffffffu, wait(BAR(B_LSUM), 0, st, limit, W_LSUM)) && alive;
+        if (alive) {
+          const float m1a = lpart[ra], l1a = lpart[BM + ra], m1b = lpart[rb], l1b = lpart[BM + rb];
+          const float ma = fmaxf(m_a, m1a), mb = fmaxf(m_b, m1b);
+          l_a = (m_a == -INFINITY ? 0.f : l_a * ex2(m_a - ma)) + (m1a == -INFINITY ? 0.f : l1a * ex2(m1a - ma));
+          l_b = (m_b == -INFINITY ? 0.f : l_b * ex2(m_b - mb)) + (m1b == -INFINITY ? 0.f : l1b * ex2(m1b - mb));
+          m_a = ma;
+          m_b = mb;
+        }
+      }
+      if (ok && alive && c == 0 && par == 0) {
         const long long rows = (long long)a.B * a.N * a.H;
 #pragma unroll
         for (int rsel = 0; rsel < 2; ++rsel) {
@@ -672,11 +738,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
 
     // ---- epilogue: unnormalised partial o_lat half of rows 32q .. 32q+31 ----------------
     // (.32x32b: thread = row; the sender warp writes O columns 0..127, the softmax 128..255)
-    if (alive && nt > 0)
+    if (alive && nt > 0 && par == 0)
       alive = __all_sync(0xffffffffu, wait(BAR(B_O_FULL), 0, st, limit, W_O_FULL));
     const int r = 32 * q + lane;
     const int rr = rt * BM + r;
-    if (ok && alive && nt > 0) {
+    if (ok && alive && nt > 0 && par == 0) {
       const long long rows = (long long)a.B * a.N * a.H;
       const int g = is_softmax ? 1 : 0;
       float* po = a.part_o + ((long long)s * rows + req_row0 + (rr < nrows ? rr : 0)) * a.d_c +
