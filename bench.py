@@ -39,7 +39,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture of that workload (profiles/attn_tc_kernel_<workload>.md), keyed by
 # the SHA-256 of the kernel source the capture was taken on: a changed kernel
 # reports null until it is captured again.
-ATTN_TRAFFIC = {}
+ATTN_TRAFFIC = {
+    "kimi_single": ("58352b7385c8aed51bca8c6b7cf443084794828645df2ae9089c12415d2ba310", 9626880),
+}
 
 
 def attn_traffic(workload):
