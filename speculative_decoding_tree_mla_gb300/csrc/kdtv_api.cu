@@ -60,9 +60,36 @@ int make_plan(const kdtv_dims* d, Plan* p) {
   p->t_cap = d->page_size ? d->max_pages * d->page_size : d->t_stride;
   const int sms = sm_count() > 0 ? sm_count() : 152;   // no device: size for a GB300
   p->sms = sms;
-  int chunk;
+  const size_t rows = (size_t)p->rows;
+  size_t off = kStatusBytes;
   if (p->tensor_core) {
-    chunk = tc_chunk(d, sms);
+    // Stream-K: one CTA pair per two SMs, each taking W consecutive 64-key
+    // units of the (request, row tile, key tile) sequence; W is at least
+    // wmin so that a row tile is cut into at most 63 pieces (the combine
+    // kernel merges up to 64 partials per row).
+    p->rt_count = (d->N * d->H + 127) / 128;
+    const long long R = (long long)d->B * p->rt_count;
+    const long long u_cap = (p->t_cap + 63) / 64;
+    p->sk_wmin = (int)((u_cap + 61) / 62);
+    if (p->sk_wmin < 1) p->sk_wmin = 1;
+    p->sk_wforce = d->kv_chunk > 0 ? (d->kv_chunk + 63) / 64 : 0;
+    long long clusters = sms / 2 > 0 ? sms / 2 : 1;
+    if (p->sk_wforce > 0) {
+      const long long w = p->sk_wforce > p->sk_wmin ? p->sk_wforce : p->sk_wmin;
+      const long long need = (R * u_cap + w - 1) / w;
+      if (need > clusters) clusters = need;
+    }
+    if (clusters > (1 << 20) || R * u_cap >= (1ll << 30)) return KDTV_ERR_UNSUPPORTED;
+    p->sk_clusters = (int)clusters;
+    p->slots = (int)(R + clusters + 1);
+    p->chunk = 64;
+    p->splits = 1;
+    p->off_qlat = off;    off = align256(off + rows * d->d_c * sizeof(float));
+    p->off_part_o = off;  off = align256(off + (size_t)p->slots * 128 * d->d_c * sizeof(float));
+    p->off_part_ml = off; off = align256(off + (size_t)p->slots * 128 * 2 * sizeof(float));
+    p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
+    p->off_sk = off;      off = align256(off + (size_t)(kSkHeader + 3 * R) * sizeof(int));
+    p->off_anc = off;     off = align256(off + (size_t)d->B * d->N * 4 * sizeof(uint32_t));
   } else {
     p->heads_per_cta = d->H < 16 ? d->H : 16;
     long long base = (long long)d->B * d->N * ((d->H + p->heads_per_cta - 1) / p->heads_per_cta);
@@ -70,19 +97,17 @@ int make_plan(const kdtv_dims* d, Plan* p) {
     long long max_s = (p->t_cap + 63) / 64;
     if (want < 1) want = 1;
     if (want > max_s) want = max_s;
-    chunk = (int)((p->t_cap + want - 1) / want);
+    int chunk = (int)((p->t_cap + want - 1) / want);
     chunk = (chunk + 31) / 32 * 32;
+    if (d->kv_chunk > 0) chunk = d->kv_chunk;
+    p->chunk = chunk;
+    p->splits = (p->t_cap + chunk - 1) / chunk;
+    if (p->splits > 1024) return KDTV_ERR_UNSUPPORTED;
+    p->off_qlat = off;    off = align256(off + rows * d->d_c * sizeof(float));
+    p->off_part_o = off;  off = align256(off + (size_t)p->splits * rows * d->d_c * sizeof(float));
+    p->off_part_ml = off; off = align256(off + (size_t)p->splits * rows * 2 * sizeof(float));
+    p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
   }
-  if (d->kv_chunk > 0) chunk = d->kv_chunk;
-  p->chunk = chunk;
-  p->splits = (p->t_cap + chunk - 1) / chunk;
-  if (p->splits > 1024) return KDTV_ERR_UNSUPPORTED;
-  const size_t rows = (size_t)p->rows;
-  size_t off = kStatusBytes;
-  p->off_qlat = off;    off = align256(off + rows * d->d_c * sizeof(float));
-  p->off_part_o = off;  off = align256(off + (size_t)p->splits * rows * d->d_c * sizeof(float));
-  p->off_part_ml = off; off = align256(off + (size_t)p->splits * rows * 2 * sizeof(float));
-  p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
   p->total = off;
   return KDTV_OK;
 }
@@ -140,6 +165,14 @@ extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const vo
   a.part_o = reinterpret_cast<float*>(ws + p.off_part_o);
   a.part_ml = reinterpret_cast<float*>(ws + p.off_part_ml);
   a.o_lat = reinterpret_cast<float*>(ws + p.off_olat);
+  if (p.tensor_core) {
+    a.sk = reinterpret_cast<int*>(ws + p.off_sk);
+    a.anc_g = reinterpret_cast<uint32_t*>(ws + p.off_anc);
+    a.rt_count = p.rt_count;
+    a.sk_clusters = p.sk_clusters;
+    a.sk_wmin = p.sk_wmin;
+    a.sk_wforce = p.sk_wforce;
+  }
 
   cudaEvent_t* ev = d->phase_events;
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return KDTV_ERR_CUDA;

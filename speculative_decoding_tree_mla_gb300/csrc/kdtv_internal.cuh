@@ -42,7 +42,9 @@ struct Plan {
   int splits;             // splits per request (ceil(t_cap / chunk))
   int heads_per_cta;      // SIMT attention: heads sharing one CTA
   int sms;                // streaming multiprocessors of the current device
-  size_t off_qlat, off_part_o, off_part_ml, off_olat, total;
+  // tensor-core path (stream-K): CTA pairs, W bounds, partial slots
+  int sk_clusters, sk_wmin, sk_wforce, rt_count, slots;
+  size_t off_qlat, off_part_o, off_part_ml, off_olat, off_sk, off_anc, total;
 };
 
 // Device-side view of the call (passed by value to kernels).
@@ -65,10 +67,47 @@ struct Args {
   float* out;
   DeviceStatus* status;
   void* q_lat;            // fp32 (SIMT) or bf16 (tensor core) [rows, d_c]
-  float* part_o;          // [splits, rows, d_c]
-  float* part_ml;         // [splits, rows, 2]  (running max m, sum l)
+  float* part_o;          // [splits, rows, d_c], or [slots, 128, d_c] with a stream-K plan
+  float* part_ml;         // [splits, rows, 2] or [slots, 128, 2]  (running max m, sum l)
   float* o_lat;           // [rows, d_c]
+  // Stream-K plan of the tensor-core attention (nullptr: split layout).
+  int* sk;                // kSkHeader ints {U, W, clusters, R}, then {S_r, u_r, base_r} per row tile
+  uint32_t* anc_g;        // [B, N, 4] ancestor masks, written by the plan kernel
+  int rt_count;           // 128-row tiles per request
+  int sk_clusters;        // CTA pairs launched
+  int sk_wmin;            // lower bound on W (units per CTA pair)
+  int sk_wforce;          // forced W from kv_chunk (0 = none)
 };
+
+constexpr int kSkHeader = 4;
+
+// Where the partials of query row `row` live: `count` partial rows at part
+// row index base + k * step (k = 0 .. count-1).  With a stream-K plan the
+// row's 128-row tile r was cut into pieces at multiples of W; its pieces hold
+// consecutive slots base_r .. base_r + count - 1.
+struct PartialRef {
+  long long base, step;
+  int count;
+};
+__device__ __forceinline__ PartialRef partials_of_row(const Args& a, long long row) {
+  PartialRef p;
+  if (!a.sk) {
+    p.base = row;
+    p.step = (long long)a.B * a.N * a.H;
+    p.count = a.splits;
+    return p;
+  }
+  const int nh = a.N * a.H;
+  const int b = (int)(row / nh), rr = (int)(row % nh);
+  const int r = b * a.rt_count + rr / 128, tr = rr % 128;
+  const int W = a.sk[1];
+  const int* e = a.sk + kSkHeader + 3 * r;
+  const int S = e[0], u = e[1], base = e[2];
+  p.count = u > 0 ? 1 + ((S + u + W - 1) / W - 1 - S / W) : 0;
+  p.base = (long long)base * 128 + tr;
+  p.step = 128;
+  return p;
+}
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -167,13 +206,13 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t s,
 cudaError_t launch_absorb(const Args& a, cudaStream_t s, bool bf16_out);
 cudaError_t launch_combine_uproj(const Args& a, const Plan& p, cudaStream_t s,
                                  cudaEvent_t* ev);
-cudaError_t launch_absorb_tc(const Args& a, cudaStream_t s);
+// after_plan: may start beside the attention plan kernel (programmatic launch)
+cudaError_t launch_absorb_tc(const Args& a, cudaStream_t s, bool after_plan);
 cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t s,
                                     cudaEvent_t* ev);
 bool absorb_tc_ok(const Args& a);
 bool combine_uproj_tc_ok(const Args& a);
 int tc_supported(const kdtv_dims* d);
 int tc_launches(const kdtv_dims* d, int splits);
-int tc_chunk(const kdtv_dims* d, int sm_count);
 
 }  // namespace kdtv

@@ -208,22 +208,23 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(Args a, int G) {
   for (int g = tid; g < ng; g += blockDim.x) { ml[2 * g] = m_s[g]; ml[2 * g + 1] = l_s[g]; }
 }
 
-// o_lat[row] = sum_s e^{m_s - m*} o_s / sum_s e^{m_s - m*} l_s.
+// o_lat[row] = sum_s e^{m_s - m*} o_s / sum_s e^{m_s - m*} l_s over the row's
+// partials (split-KV ranges, or the pieces of a stream-K plan).
 __global__ void __launch_bounds__(128) combine_kernel(Args a) {
   const long long row = blockIdx.x;
-  const long long rows = (long long)a.B * a.N * a.H;
   __shared__ float w_s[1024];
   __shared__ float inv_l;
-  const int S = a.splits;
+  const PartialRef pr = partials_of_row(a, row);
+  const int S = pr.count < 1024 ? pr.count : 1024;
   if (threadIdx.x == 0) {
     float m = -INFINITY;
     for (int s = 0; s < S; ++s) {
-      const float* ml = a.part_ml + ((long long)s * rows + row) * 2;
+      const float* ml = a.part_ml + (pr.base + s * pr.step) * 2;
       if (ml[1] > 0.f) m = fmaxf(m, ml[0]);
     }
     float l = 0.f;
     for (int s = 0; s < S; ++s) {
-      const float* ml = a.part_ml + ((long long)s * rows + row) * 2;
+      const float* ml = a.part_ml + (pr.base + s * pr.step) * 2;
       float w = (ml[1] > 0.f) ? expf(ml[0] - m) : 0.f;
       w_s[s] = w;
       l += w * ml[1];
@@ -234,7 +235,7 @@ __global__ void __launch_bounds__(128) combine_kernel(Args a) {
   for (int d = threadIdx.x; d < a.d_c; d += blockDim.x) {
     float acc = 0.f;
     for (int s = 0; s < S; ++s)
-      if (w_s[s] != 0.f) acc = fmaf(w_s[s], a.part_o[((long long)s * rows + row) * a.d_c + d], acc);
+      if (w_s[s] != 0.f) acc = fmaf(w_s[s], a.part_o[(pr.base + s * pr.step) * a.d_c + d], acc);
     a.o_lat[row * a.d_c + d] = acc * inv_l;
   }
 }

@@ -6,11 +6,15 @@
 // Moment of Proof: Validating a Native CUDA Speculative Decoding Engine",
 // section "The Context: Building a Native DDTree Engine from Scratch").
 //
-// Work decomposition.  A work item is (request b, tile of 128 query rows,
-// split-KV key range).  Query rows are (node, head) pairs with the head
-// fastest, so one tile holds 128/H nodes; every row of a node shares that
-// node's ancestor mask.  An item runs on a CLUSTER OF TWO CTAs that split
-// the latent dimension:
+// Work decomposition (stream-K).  Query rows are (node, head) pairs with the
+// head fastest, cut into 128-row tiles per request; the work of a row tile is
+// its sequence of 64-key tiles.  All (request, row tile, key tile) units form
+// one sequence and CTA pair c takes the W consecutive units [cW, (c+1)W),
+// split into pieces at row-tile boundaries; each piece writes one partial
+// (m, l, o_lat) that the combine kernel merges.  A small plan kernel computes
+// the unit offsets, W and the partial slots (and each request's ancestor
+// masks) on the device, so ragged batches are spread evenly.  A pair is a
+// CLUSTER OF TWO CTAs that split the latent dimension:
 //   CTA 0 holds q_lat[:, 0:256] and q_rope, and reads c_kv[:, 0:256] + k_rope;
 //   CTA 1 holds q_lat[:, 256:512] and reads c_kv[:, 256:512].
 // Per 64-key tile each CTA computes the partial score tile S_c = Q_c K_c^T
@@ -35,13 +39,15 @@
 // four for its rescale factors.  Key tiles are also prefetched into L2 a few
 // tiles ahead of the ring.
 //
-// Warp roles (352 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
-// issues Q.K^T; warps 2-5 (one per lane quadrant) quantise and send the
-// peer's score rows; warps 6-9 (one per quadrant, four threads per row in
-// the .16x256b TMEM layout, so row maxima and sums meet by warp shuffles) run
-// the softmax of the CTA's own rows; warp 10 issues P.V.  Warps 2-9 also load
-// Q into TMEM and write the partial o_lat.  Every wait is bounded (2 s, or
-// ~20 ms with KDTV_FLAG_TEST_STALL); on timeout the kernel records
+// Warp roles (480 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
+// issues Q.K^T; warps 2-5 (one per lane quadrant) load each piece's Q into
+// TMEM and quantise and send the peer's score rows; warps 6-13 (two per
+// quadrant, taking even and odd tiles, four threads per row in the .16x256b
+// TMEM layout, so row maxima and sums meet by warp shuffles; the running
+// reference maxima pass between the two through shared memory) run the
+// softmax of the CTA's own rows and write each piece's partial o_lat; warp 14
+// issues P.V.  Every wait is bounded (2 s, or ~20 ms with
+// KDTV_FLAG_TEST_STALL); on timeout the kernel records
 // KDTV_ERR_DEVICE_TIMEOUT, lets in-flight copies land, drains its MMAs, frees
 // TMEM and returns.
 
@@ -89,12 +95,10 @@ constexpr int OFF_QR = OFF_KV + kStages * kMaxCh * kKVChunk;
 constexpr int OFF_P = OFF_QR + kQRopeBytes;
 constexpr int OFF_RX = OFF_P + kPBytes;                        // two receive buffers
 constexpr int OFF_AF = OFF_RX + 2 * kRxStride;                 // [kAfBufs][BM] floats
-constexpr int OFF_ANC = OFF_AF + kAfBufs * BM * 4;
-constexpr int OFF_PAR = OFF_ANC + kMaxNodes * 16;              // staged parent[]
-constexpr int OFF_MREF = OFF_PAR + kMaxNodes * 4;              // [2 parities][BM] reference maxima
+constexpr int OFF_MREF = OFF_AF + kAfBufs * BM * 4;             // [2 parities][BM] reference maxima
 constexpr int OFF_LPART = OFF_MREF + 2 * BM * 4;                // [m | l][BM] of the odd-tile warps
 constexpr int OFF_BAR = OFF_LPART + 2 * BM * 4;
-constexpr int kNumBars = 40;
+constexpr int kNumBars = 48;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -121,18 +125,76 @@ enum Bar : int {
   B_STALL = B_MMA_DONE + 1,
   B_MREF = B_STALL + 1,              // [2 parities][4 quadrants] reference maxima published
   B_LSUM = B_MREF + 8,               // the odd-tile softmax warps published their (m, l)
-  B_COUNT = B_LSUM + 1
+  B_Q_EMPTY = B_LSUM + 1,            // Q.K^T of a piece completed: TMEM Q may be reloaded
+  B_QR_EMPTY = B_Q_EMPTY + 1,        // ... and q_rope (CTA 0)
+  B_O_FREE = B_QR_EMPTY + 1,         // the softmax warps wrote a piece's O out
+  B_L_FREE = B_O_FREE + 1,           // the even-tile warps read the odd-tile (m, l)
+  B_COUNT = B_L_FREE + 1
 };
 static_assert(B_COUNT <= kNumBars, "barrier slots");
 
 // Wait sites (reported as the timeout detail).
 enum Site { W_Q = 1, W_KV_FULL, W_KV_EMPTY, W_P_FULL, W_S_FULL, W_TX_OK, W_RX_FULL,
-            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_AF, W_P_RX, W_MREF, W_LSUM };
+            W_P_EMPTY, W_O_FULL, W_STALL, W_DRAIN, W_S_FREE, W_AF, W_P_RX, W_MREF, W_LSUM,
+            W_Q_EMPTY, W_O_FREE };
 
 struct TcCfg {
-  int row_tiles;               // ceil(N * H / 128)
   unsigned long long limit_ns; // bound on every wait
 };
+
+// ---- stream-K pieces ---------------------------------------------------------------------
+// A piece: key tiles [t0, t1) of row tile r (request b, tile rt of it),
+// written to partial slot `slot`; L is the request's prefix length.
+struct Piece {
+  int r, b, rt, t0, t1, slot, L;
+};
+
+__device__ __forceinline__ const int* sk_row(const Args& a, int r) { return a.sk + kSkHeader + 3 * r; }
+
+__device__ __forceinline__ void piece_fill(const Args& a, int r, int beg, int end, int W, Piece& p) {
+  const int* e = sk_row(a, r);
+  p.r = r;
+  p.b = r / a.rt_count;
+  p.rt = r - p.b * a.rt_count;
+  p.t0 = beg - e[0];
+  p.t1 = min(end, e[0] + e[1]) - e[0];
+  p.slot = e[2] + (beg / W - e[0] / W);   // the first piece of r starts at S_r
+  p.L = a.prefix_len[p.b];
+}
+
+// First piece of the unit range [beg, end); false if the range is empty.
+__device__ bool piece_first(const Args& a, int beg, int end, int W, Piece& p) {
+  if (beg >= end) return false;
+  const int R = a.sk[3];
+  int lo = 0, hi = R - 1;                     // last row tile starting at or before beg
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sk_row(a, mid)[0] <= beg) lo = mid; else hi = mid - 1;
+  }
+  int r = lo;
+  while (r < R && sk_row(a, r)[0] + sk_row(a, r)[1] <= beg) ++r;
+  if (r >= R) return false;
+  piece_fill(a, r, beg, end, W, p);
+  return true;
+}
+
+// The piece after p (it starts at the next non-empty row tile); false at the end.
+__device__ bool piece_next(const Args& a, int end, int W, Piece& p) {
+  const int R = a.sk[3];
+  const int u = sk_row(a, p.r)[0] + p.t1;
+  if (u >= end) return false;
+  int r = p.r + 1;
+  while (r < R && sk_row(a, r)[1] == 0) ++r;
+  if (r >= R) return false;
+  piece_fill(a, r, u, end, W, p);
+  return true;
+}
+
+// Keeps a value computed before the next wait: the compiler may otherwise
+// sink arithmetic whose result is only used after a wait below it, onto the
+// critical path that the wait ends.
+__device__ __forceinline__ void pin(uint32_t& x) { asm volatile("" : "+r"(x)); }
+__device__ __forceinline__ void pin(float& x) { asm volatile("" : "+f"(x)); }
 
 // 2^e as a float for e in [-126, 127] (exact).
 __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
@@ -173,6 +235,52 @@ __device__ __forceinline__ void rescale_o_rows(uint32_t taddr, float alpha_a, fl
   }
 }
 
+// Stores 32 * nch32 O columns of the 32 rows of a warp's TMEM lane quadrant
+// (ta0: TMEM address of the quadrant's first lane and column; dst0: row 0,
+// column 0 of the destination, rows d_c floats apart; rows >= nvalid are
+// skipped).  Reads the .16x256b layout (rows t/4 and t/4 + 8 of each 16-row
+// half, column pairs 8k + 2c); a pair exchange between threads c and c ^ 1
+// gives each thread 4 consecutive columns, so one warp store covers 64
+// contiguous bytes of each of 8 rows.  Out of line: it runs once per piece.
+__device__ __noinline__ void store_o_quadrant(uint32_t ta0, float* dst0, int d_c, int nvalid, int nch32) {
+  const int lane = threadIdx.x & 31, c = lane & 3;
+  const bool odd = c & 1;
+#pragma unroll 1
+  for (int hh = 0; hh < 2; ++hh) {
+    const int r = 16 * hh + (lane >> 2);                 // rows r, r + 8
+    const bool wa = r < nvalid, wb = r + 8 < nvalid;
+    float* pra = dst0 + (long long)r * d_c + (odd ? 2 * c + 6 : 2 * c);
+    float* prb = pra + 8 * d_c;
+    const uint32_t ta = ta0 + (static_cast<uint32_t>(16 * hh) << 16);
+#pragma unroll 1
+    for (int cc = 0; cc < nch32; ++cc) {                 // 32 columns per load
+      uint32_t v[16];
+      tmem_ld_16x256b_x4(ta + 32 * cc, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 4; k += 2) {
+        // rows a (v[4k], v[4k+1]) and b (v[4k+2], v[4k+3]) of pairs k, k+1
+        const uint32_t sa0 = odd ? v[4 * k] : v[4 * k + 4], sa1 = odd ? v[4 * k + 1] : v[4 * k + 5];
+        const uint32_t sb0 = odd ? v[4 * k + 2] : v[4 * k + 6], sb1 = odd ? v[4 * k + 3] : v[4 * k + 7];
+        const uint32_t ra0 = __shfl_xor_sync(0xffffffffu, sa0, 1);
+        const uint32_t ra1 = __shfl_xor_sync(0xffffffffu, sa1, 1);
+        const uint32_t rb0 = __shfl_xor_sync(0xffffffffu, sb0, 1);
+        const uint32_t rb1 = __shfl_xor_sync(0xffffffffu, sb1, 1);
+        const float4 oa = odd ? make_float4(__uint_as_float(ra0), __uint_as_float(ra1),
+                                            __uint_as_float(v[4 * k + 4]), __uint_as_float(v[4 * k + 5]))
+                              : make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
+                                            __uint_as_float(ra0), __uint_as_float(ra1));
+        const float4 ob = odd ? make_float4(__uint_as_float(rb0), __uint_as_float(rb1),
+                                            __uint_as_float(v[4 * k + 6]), __uint_as_float(v[4 * k + 7]))
+                              : make_float4(__uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]),
+                                            __uint_as_float(rb0), __uint_as_float(rb1));
+        if (wa) *reinterpret_cast<float4*>(pra + 32 * cc + 8 * k) = oa;
+        if (wb) *reinterpret_cast<float4*>(prb + 32 * cc + 8 * k) = ob;
+      }
+    }
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                const __grid_constant__ CUtensorMap tm_ckv,
@@ -184,22 +292,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
-  const int item = blockIdx.x >> 1;
-  const int rt = item % cfg.row_tiles;
-  const int s = (item / cfg.row_tiles) % a.splits;
-  const int b = item / (cfg.row_tiles * a.splits);
-  const int nch = rank == 0 ? 5 : 4;
-  uint32_t* anc = reinterpret_cast<uint32_t*>(sm + OFF_ANC);
+  const int cl = blockIdx.x >> 1;                  // this CTA pair
   volatile int* misc = reinterpret_cast<volatile int*>(sm + OFF_MISC);
   auto BAR = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
   DeviceStatus* st = a.status;
   const uint64_t limit = cfg.limit_ns;
   grid_dep_launch();   // the combine kernel may start its weight loads early
 
-  // ---- prologue: barriers, validation, ancestor masks, TMEM ------------------------
+  // ---- prologue: barriers, TMEM ------------------------------------------------------
   if (tid == 0) {
     mbar_init(BAR(B_QR_FULL), 1);
-    mbar_init(BAR(B_Q_READY), 8);
+    mbar_init(BAR(B_Q_READY), 4);         // the 4 sender warps stored Q
     for (int i = 0; i < kStages; ++i) {
       mbar_init(BAR(B_KV_FULL + i), 1);
       mbar_init(BAR(B_KV_EMPTY + i), 1);
@@ -211,7 +314,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       mbar_init(BAR(B_TX_OK + i), 4);     // one relaxed arrival per peer softmax warp
     }
     for (int i = 0; i < kAfBufs; ++i) mbar_init(BAR(B_AF_FULL + i), 1);
-    mbar_init(BAR(B_P_FULL), 4);          // our 4 softmax warps
+    mbar_init(BAR(B_P_FULL), 4);          // the tile's 4 softmax warps
     mbar_init(BAR(B_P_RX), 1);            // armed with expect_tx; filled by the peer's bulk copies
     // P.V commits of both CTAs (multicast), one barrier per tile parity: each
     // softmax warp waits only for the other parity's tiles, so it sees every
@@ -223,38 +326,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     mbar_init(BAR(B_STALL), 1);
     for (int i = 0; i < 8; ++i) mbar_init(BAR(B_MREF + i), 1);
     mbar_init(BAR(B_LSUM), 4);
+    mbar_init(BAR(B_Q_EMPTY), 1);
+    mbar_init(BAR(B_QR_EMPTY), 1);
+    mbar_init(BAR(B_O_FREE), 4);          // the 4 softmax warps that wrote a piece's O out
+    mbar_init(BAR(B_L_FREE), 4);          // the even-tile warps read the hand-over
     mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchanges of tiles 0 and 1
     mbar_expect_tx(BAR(B_RX_FULL + 1), kRxBytes);
     for (int i = 0; i < kAfBufs; ++i) mbar_expect_tx(BAR(B_AF_FULL + i), kAfBytes);
     mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes);
     fence_mbar_init();
-    int L = 0;
-    int ok = prefix_ok(a, b, &L) ? 1 : 0;
-    if (ok && a.page_size) {
-      const int T = L + a.N;
-      const int k0 = s * a.chunk, k1 = min(T, k0 + a.chunk);
-      for (int p = k0 / a.page_size; k0 < k1 && p <= (k1 - 1) / a.page_size; ++p) {
-        int page = a.page_table[(long long)b * a.max_pages + p];
-        if (page < 0 || page >= a.num_pages) {
-          record_error(st, KDTV_ERR_BAD_PAGE, (unsigned)b);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    misc[1] = ok;
-    misc[2] = L;
-    misc[3] = 1;   // tree ok until a walker says otherwise
-  }
-  int32_t* par_s = reinterpret_cast<int32_t*>(sm + OFF_PAR);
-  if (tid < a.N) par_s[tid] = a.parent[(long long)b * a.N + tid];
-  __syncthreads();
-  if (tid < a.N) {
-    uint32_t m[4];
-    bool good = ancestor_mask_smem(a, b, par_s, tid, m);
-    anc[4 * tid + 0] = m[0]; anc[4 * tid + 1] = m[1];
-    anc[4 * tid + 2] = m[2]; anc[4 * tid + 3] = m[3];
-    if (!good) misc[3] = 0;
   }
   if (warp == 1) {
     tmem_alloc(sbase + OFF_MISC, kTmemCols);
@@ -265,89 +345,118 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
   tc_fence_after();
   cluster_sync();   // the peer's barriers are initialised before any remote access
 
+  // The plan, the ancestor masks and q_lat are written by the kernels before
+  // this one.  The pair's unit range is [beg, end).
+  grid_dep_wait();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
-  const bool ok = misc[1] && misc[3];
-  const int L = misc[2];
-  const int T = L + a.N;
-  const int k0 = s * a.chunk;
-  const int k1 = min(T, k0 + a.chunk);
-  const int nt = (ok && k1 > k0) ? (k1 - k0 + BN - 1) / BN : 0;
-  const long long req_row0 = (long long)b * a.N * a.H;    // first global row of request b
   const int nrows = a.N * a.H;
+  const int U = a.sk[0], W = a.sk[1];
+  const long long beg_ll = (long long)cl * W;
+  const int beg = beg_ll < U ? (int)beg_ll : U;
+  const int end = (long long)beg + W < U ? beg + W : U;
+  const int G = end - beg;                         // key tiles of this pair
 
   if (warp == 0) {
     // ---- TMA producer --------------------------------------------------------------
-    if (lane == 0 && nt > 0) {
+    if (lane == 0 && G > 0) {
       prefetch_tmap(&tm_ckv);
-      const int qrow = (int)(req_row0 + (long long)rt * BM);
-      if (rank == 0) {
-        mbar_expect_tx(BAR(B_QR_FULL), kQRopeBytes);
-        tma_load_2d(sbase + OFF_QR, &tm_qrope, BAR(B_QR_FULL), 0, qrow);
-      }
-      // Cache row of key tile j (paged: through the page table).
-      auto tile_row = [&](int j) -> int {
-        const int t0 = k0 + j * BN;
-        return a.page_size ? a.page_table[(long long)b * a.max_pages + t0 / a.page_size] * a.page_size
-                           : b * a.t_stride + t0;
+      // Cache row of key k of request b (paged: through the page table; a page
+      // id outside [0, num_pages) is reported and read as page 0).
+      auto key_row = [&](int b, int k) -> int {
+        if (!a.page_size) return b * a.t_stride + k;
+        const int page = a.page_table[(long long)b * a.max_pages + k / a.page_size];
+        if (page < 0 || page >= a.num_pages) {
+          record_error(st, KDTV_ERR_BAD_PAGE, (unsigned)b);
+          return 0;
+        }
+        return page * a.page_size;
       };
-      auto prefetch = [&](int j) {
-        const int row = tile_row(j);
+      auto prefetch = [&](int b, int k) {
+        const int row = key_row(b, k);
         for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_ckv, (int)rank * kHalf + c * CH, row);
         if (rank == 0) tma_prefetch_2d(&tm_krope, 0, row);
       };
-      for (int j = kStages; j < kStages + kPrefetch && j < nt; ++j) prefetch(j);
-      int issued = 0;
-      for (int j = 0; j < nt; ++j) {
-        const int stg = j % kStages;
-        if (j >= kStages &&
-            !wait(BAR(B_KV_EMPTY + stg), ((j / kStages) - 1) & 1, st, limit, W_KV_EMPTY))
-          break;
-        const int row = tile_row(j);
-        mbar_expect_tx(BAR(B_KV_FULL + stg), nch * kKVChunk);
-        const uint32_t dst = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
-        for (int c = 0; c < 4; ++c)
-          tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
-                      (int)rank * kHalf + c * CH, row);
-        if (rank == 0) tma_load_2d(dst + 4 * kKVChunk, &tm_krope, BAR(B_KV_FULL + stg), 0, row);
-        issued = j + 1;
-        if (j + kStages + kPrefetch < nt) prefetch(j + kStages + kPrefetch);
+      Piece pc;
+      bool have = piece_first(a, beg, end, W, pc);
+      int g = 0, pi = 0, issued = 0, qr_issued = 0;
+      bool alive = true;
+      while (alive && have) {
+        if (rank == 0) {   // q_rope rows of this piece, once Q.K^T of the previous piece is done
+          if (pi >= 1 && !wait(BAR(B_QR_EMPTY), (pi - 1) & 1, st, limit, W_Q_EMPTY)) break;
+          ++qr_issued;
+          mbar_expect_tx(BAR(B_QR_FULL), kQRopeBytes);
+          tma_load_2d(sbase + OFF_QR, &tm_qrope, BAR(B_QR_FULL), 0,
+                      (int)((long long)pc.b * nrows + pc.rt * BM));
+        }
+        for (int j = pc.t0 + kStages; j < pc.t0 + kStages + kPrefetch && j < pc.t1; ++j)
+          prefetch(pc.b, j * BN);
+        for (int j = pc.t0; j < pc.t1; ++j, ++g) {
+          const int stg = g % kStages;
+          if (g >= kStages &&
+              !wait(BAR(B_KV_EMPTY + stg), ((g / kStages) - 1) & 1, st, limit, W_KV_EMPTY)) {
+            alive = false;
+            break;
+          }
+          const int row = key_row(pc.b, j * BN);
+          mbar_expect_tx(BAR(B_KV_FULL + stg), (rank == 0 ? 5 : 4) * kKVChunk);
+          const uint32_t dst = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+          for (int c = 0; c < 4; ++c)
+            tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
+                        (int)rank * kHalf + c * CH, row);
+          if (rank == 0) tma_load_2d(dst + 4 * kKVChunk, &tm_krope, BAR(B_KV_FULL + stg), 0, row);
+          issued = g + 1;
+          if (j + kStages + kPrefetch < pc.t1) prefetch(pc.b, (j + kStages + kPrefetch) * BN);
+        }
+        ++pi;
+        have = piece_next(a, end, W, pc);
       }
       // Drain: every issued copy has landed before this CTA may exit.
-      if (rank == 0) wait(BAR(B_QR_FULL), 0, st, limit, W_DRAIN);
+      if (qr_issued >= 1) wait(BAR(B_QR_FULL), (qr_issued - 1) & 1, st, limit, W_DRAIN);
       for (int j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
         wait(BAR(B_KV_FULL + j % kStages), (j / kStages) & 1, st, limit, W_DRAIN);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---- Q.K^T issuer (also owns TMEM) ------------------------------------------------
-    if (lane == 0 && nt > 0) {
+    if (lane == 0 && G > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, 0, 0);
-      bool alive = wait(BAR(B_Q_READY), 0, st, limit, W_Q);
-      if (alive && rank == 0) alive = wait(BAR(B_QR_FULL), 0, st, limit, W_Q);
-      for (int j = 0; alive && j < nt; ++j) {
-        const int stg = j % kStages, buf = j & 1;
-        alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
-        // the score buffer is rewritten: senders and softmax must have read tile j-2
-        if (alive && j >= 2)
-          alive = wait(BAR(B_S_FREE + buf), ((j >> 1) - 1) & 1, st, limit, W_S_FREE);
-        if (!alive) break;
-        tc_fence_after();
-        const uint32_t d = tmem + kColS + 64 * buf;
-        const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+      Piece pc;
+      bool have = piece_first(a, beg, end, W, pc);
+      int g = 0, pi = 0;
+      bool alive = true;
+      while (alive && have) {
+        alive = wait(BAR(B_Q_READY), pi & 1, st, limit, W_Q);
+        if (alive && rank == 0) alive = wait(BAR(B_QR_FULL), pi & 1, st, limit, W_Q);
+        for (int j = pc.t0; alive && j < pc.t1; ++j, ++g) {
+          const int stg = g % kStages, buf = g & 1;
+          alive = wait(BAR(B_KV_FULL + stg), (g / kStages) & 1, st, limit, W_KV_FULL);
+          // the score buffer is rewritten: senders and softmax must have read tile g-2
+          if (alive && g >= 2)
+            alive = wait(BAR(B_S_FREE + buf), ((g >> 1) - 1) & 1, st, limit, W_S_FREE);
+          if (!alive) break;
+          tc_fence_after();
+          const uint32_t d = tmem + kColS + 64 * buf;
+          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
 #pragma unroll
-        for (int kk = 0; kk < kHalf / 16; ++kk) {       // latent half: A = q_lat in TMEM
-          uint64_t bd = smem_desc(kv + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
-          mma_bf16_ts(d, tmem + kColQ + 8 * kk, bd, kIdescQK, kk > 0);
-        }
-        if (rank == 0) {
-#pragma unroll
-          for (int kk = 0; kk < CH / 16; ++kk) {        // rope: A = q_rope in smem
-            uint64_t ad = smem_desc(sbase + OFF_QR + kk * 32, 16, 1024);
-            uint64_t bd = smem_desc(kv + 4 * kKVChunk + kk * 32, 16, 1024);
-            mma_bf16(d, ad, bd, kIdescQK, 1);
+          for (int kk = 0; kk < kHalf / 16; ++kk) {     // latent half: A = q_lat in TMEM
+            uint64_t bd = smem_desc(kv + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ts(d, tmem + kColQ + 8 * kk, bd, kIdescQK, kk > 0);
           }
+          if (rank == 0) {
+#pragma unroll
+            for (int kk = 0; kk < CH / 16; ++kk) {      // rope: A = q_rope in smem
+              uint64_t ad = smem_desc(sbase + OFF_QR + kk * 32, 16, 1024);
+              uint64_t bd = smem_desc(kv + 4 * kKVChunk + kk * 32, 16, 1024);
+              mma_bf16(d, ad, bd, kIdescQK, 1);
+            }
+          }
+          mma_commit(BAR(B_S_FULL + buf));
         }
-        mma_commit(BAR(B_S_FULL + buf));
+        if (!alive) break;
+        mma_commit(BAR(B_Q_EMPTY));                 // Q (and q_rope) may be reloaded
+        if (rank == 0) mma_commit(BAR(B_QR_EMPTY));
+        ++pi;
+        have = piece_next(a, end, W, pc);
       }
       mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
       wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
@@ -355,33 +464,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     __syncwarp();
   } else if (warp == kWarpPV) {
     // ---- P.V issuer: O_c += P . c_kv[:, 256c : 256c+256] ------------------------------
-    if (lane == 0 && nt > 0) {
+    if (lane == 0 && G > 0) {
       constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
+      Piece pc;
+      bool have = piece_first(a, beg, end, W, pc);
+      int g = 0, pi = 0, p_armed = 1;              // phases of B_P_RX armed so far
       bool alive = true;
-      int p_armed = 1;                             // phases of B_P_RX armed so far
-      for (int j = 0; j < nt; ++j) {
-        const int stg = j % kStages;
-        alive = wait(BAR(B_P_FULL), j & 1, st, limit, W_P_FULL);
-        if (alive) alive = wait(BAR(B_P_RX), j & 1, st, limit, W_P_RX);
-        // already complete (Q.K^T of tile j read this stage); orders the TMA data
-        if (alive) alive = wait(BAR(B_KV_FULL + stg), (j / kStages) & 1, st, limit, W_KV_FULL);
-        if (!alive) break;
-        // arm the peer's P rows of tile j+1 before our commit lets the peer send them
-        if (j + 1 < nt) { mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes); ++p_armed; }
-        tc_fence_after();
-        const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+      while (alive && have) {
+        for (int j = pc.t0; j < pc.t1; ++j, ++g) {
+          const int stg = g % kStages;
+          alive = wait(BAR(B_P_FULL), g & 1, st, limit, W_P_FULL);
+          if (alive) alive = wait(BAR(B_P_RX), g & 1, st, limit, W_P_RX);
+          // already complete (Q.K^T of tile g read this stage); orders the TMA data
+          if (alive) alive = wait(BAR(B_KV_FULL + stg), (g / kStages) & 1, st, limit, W_KV_FULL);
+          // the first P.V of a piece overwrites O: the previous piece must be written out
+          if (alive && j == pc.t0 && pi >= 1)
+            alive = wait(BAR(B_O_FREE), (pi - 1) & 1, st, limit, W_O_FREE);
+          if (!alive) break;
+          // arm the peer's P rows of tile g+1 before our commit lets the peer send them
+          if (g + 1 < G) { mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes); ++p_armed; }
+          tc_fence_after();
+          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // A = P (K-major, 128B rows); B = V = c_kv columns of this CTA,
-          // MN-major: 64-column chunks kKVChunk apart (LBO), 8-key groups 1 KiB apart (SBO).
-          uint64_t ad = smem_desc(sbase + OFF_P + kk * 32, 16, 1024);
-          uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
-          mma_bf16(tmem + kColO, ad, bd, kIdescPV, (j > 0 || kk > 0));
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            // A = P (K-major, 128B rows); B = V = c_kv columns of this CTA,
+            // MN-major: 64-column chunks kKVChunk apart (LBO), 8-key groups 1 KiB apart (SBO).
+            uint64_t ad = smem_desc(sbase + OFF_P + kk * 32, 16, 1024);
+            uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
+            mma_bf16(tmem + kColO, ad, bd, kIdescPV, (j > pc.t0 || kk > 0));
+          }
+          mma_commit(BAR(B_KV_EMPTY + stg));
+          mma_commit_multicast(BAR(B_P_EMPTY + (g & 1)), 0x3);   // both CTAs may overwrite P
         }
-        mma_commit(BAR(B_KV_EMPTY + stg));
-        mma_commit_multicast(BAR(B_P_EMPTY + (j & 1)), 0x3);   // both CTAs may overwrite P
+        if (!alive) break;
+        mma_commit(BAR(B_O_FULL));                 // the piece's O is complete
+        ++pi;
+        have = piece_next(a, end, W, pc);
       }
-      if (alive) mma_commit(BAR(B_O_FULL));
       // After an abort: let the peer's P rows of an armed, unconsumed phase land.
       if (!alive && p_armed > 0) drain_wait(BAR(B_P_RX), (p_armed - 1) & 1, 200000ull);
       mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
@@ -401,363 +520,405 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     const uint32_t lane_peer = static_cast<uint32_t>(peer_base) << 16;
     const uint32_t lane32 = static_cast<uint32_t>(32 * q) << 16;
     bool alive = true;
-
-    if (nt > 0 && par == 0) {
-      grid_dep_wait();   // q_lat is written by the absorb kernel
-      // Q half of tile row 32q + lane -> TMEM [kColQ, +128) as bf16 pairs
-      // (.32x32b layout); the sender warp stores words 0..63, the even-tile softmax
-      // warp 64..127.
-      const int rq = rt * BM + 32 * q + lane;
-      const bool vq = rq < nrows;
-      const int g = is_softmax ? 1 : 0;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const __nv_bfloat16*>(a.q_lat) + (req_row0 + (vq ? rq : 0)) * 512 +
-          rank * kHalf + 128 * g);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t w[32];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          uint4 x = vq ? src[8 * h + v] : make_uint4(0u, 0u, 0u, 0u);
-          w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
-        }
-        tmem_st32u(tmem + lane32 + kColQ + 64 * g + 32 * h, w);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_Q_READY));
-    }
+    Piece pc;
+    bool have = piece_first(a, beg, end, W, pc);
 
     if (!is_softmax) {
-      // ---- sender: the peer's score rows -> the peer's receive buffer ---------------
-      for (int j = 0; alive && j < nt; ++j) {
-        const int buf = j & 1;
-        alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
-        if (!alive) break;
-        tc_fence_after();
-        uint32_t v[32];
-        tmem_ld_16x256b_x8(tmem + lane_peer + kColS + 64 * buf, v);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));
-        // one power-of-two scale per row: the row's 64 values are spread over
-        // the 4 threads t with the same t / 4
-        float ma = 0.f, mb = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          ma = max3f(ma, fabsf(__uint_as_float(v[4 * k])), fabsf(__uint_as_float(v[4 * k + 1])));
-          mb = max3f(mb, fabsf(__uint_as_float(v[4 * k + 2])), fabsf(__uint_as_float(v[4 * k + 3])));
-        }
-        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
-        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
-        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-        const int sha = fp16_shift(ma), shb = fp16_shift(mb);
-        const float sca = pow2f(sha), scb = pow2f(shb);
-        uint32_t w[16];                            // rows a then b, key pairs 8k + 2c
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          __half2 ha = __floats2half2_rn(__uint_as_float(v[4 * k]) * sca,
-                                         __uint_as_float(v[4 * k + 1]) * sca);
-          __half2 hb = __floats2half2_rn(__uint_as_float(v[4 * k + 2]) * scb,
-                                         __uint_as_float(v[4 * k + 3]) * scb);
-          w[k] = *reinterpret_cast<uint32_t*>(&ha);
-          w[8 + k] = *reinterpret_cast<uint32_t*>(&hb);
-        }
-        // the peer has consumed what we sent into this receive buffer two tiles ago
-        if (j >= 2) {
-          alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK + buf), ((j >> 1) - 1) & 1, st, limit,
-                                               W_TX_OK));
+      // ---- sender: each piece's Q into TMEM; the peer's score rows -> its receive buffer --
+      int g = 0, pi = 0;
+      while (alive && have) {
+        // Q of this piece (row 32q + lane, 256 latent columns of this CTA's half as
+        // 128 bf16 pairs, .32x32b layout) once Q.K^T of the previous piece is done.
+        if (pi >= 1) {
+          alive = __all_sync(0xffffffffu, wait(BAR(B_Q_EMPTY), (pi - 1) & 1, st, limit, W_Q_EMPTY));
           if (!alive) break;
         }
-        const uint32_t rxp = mapa(sbase + OFF_RX + buf * kRxStride, peer);
-        const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL + buf), peer);
+        {
+          const int rq = pc.rt * BM + 32 * q + lane;
+          const bool vq = rq < nrows;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              static_cast<const __nv_bfloat16*>(a.q_lat) +
+              ((long long)pc.b * nrows + (vq ? rq : 0)) * 512 + rank * kHalf);
+          tc_fence_after();
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          st_async_v4u(rxp + ((q * 4 + m) * 32 + lane) * 16, w[4 * m], w[4 * m + 1], w[4 * m + 2],
-                       w[4 * m + 3], rxfull_remote);
-        st_async_u32(rxp + kRxData + (q * 32 + lane) * 4,
-                     ((uint32_t)sha & 0xffffu) | ((uint32_t)shb << 16), rxfull_remote);
+          for (int h = 0; h < 4; ++h) {
+            uint32_t w[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              uint4 x = vq ? src[8 * h + v] : make_uint4(0u, 0u, 0u, 0u);
+              w[4 * v] = x.x; w[4 * v + 1] = x.y; w[4 * v + 2] = x.z; w[4 * v + 3] = x.w;
+            }
+            tmem_st32u(tmem + lane32 + kColQ + 32 * h, w);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_Q_READY));
+        }
+        for (int j = pc.t0; alive && j < pc.t1; ++j, ++g) {
+          const int buf = g & 1;
+          alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (g >> 1) & 1, st, limit, W_S_FULL));
+          if (!alive) break;
+          tc_fence_after();
+          uint32_t v[32];
+          tmem_ld_16x256b_x8(tmem + lane_peer + kColS + 64 * buf, v);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));
+          // one power-of-two scale per row: the row's 64 values are spread over
+          // the 4 threads t with the same t / 4
+          float ma = 0.f, mb = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            ma = max3f(ma, fabsf(__uint_as_float(v[4 * k])), fabsf(__uint_as_float(v[4 * k + 1])));
+            mb = max3f(mb, fabsf(__uint_as_float(v[4 * k + 2])), fabsf(__uint_as_float(v[4 * k + 3])));
+          }
+          ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+          mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+          ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+          mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+          const int sha = fp16_shift(ma), shb = fp16_shift(mb);
+          const float sca = pow2f(sha), scb = pow2f(shb);
+          uint32_t w[16];                          // rows a then b, key pairs 8k + 2c
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            __half2 ha = __floats2half2_rn(__uint_as_float(v[4 * k]) * sca,
+                                           __uint_as_float(v[4 * k + 1]) * sca);
+            __half2 hb = __floats2half2_rn(__uint_as_float(v[4 * k + 2]) * scb,
+                                           __uint_as_float(v[4 * k + 3]) * scb);
+            w[k] = *reinterpret_cast<uint32_t*>(&ha);
+            w[8 + k] = *reinterpret_cast<uint32_t*>(&hb);
+          }
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pin(w[k]);
+          // the peer has consumed what we sent into this receive buffer two tiles ago
+          if (g >= 2) {
+            alive = __all_sync(0xffffffffu, wait(BAR(B_TX_OK + buf), ((g >> 1) - 1) & 1, st, limit,
+                                                 W_TX_OK));
+            if (!alive) break;
+          }
+          const uint32_t rxp = mapa(sbase + OFF_RX + buf * kRxStride, peer);
+          const uint32_t rxfull_remote = mapa(BAR(B_RX_FULL + buf), peer);
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            st_async_v4u(rxp + ((q * 4 + m) * 32 + lane) * 16, w[4 * m], w[4 * m + 1], w[4 * m + 2],
+                         w[4 * m + 3], rxfull_remote);
+          st_async_u32(rxp + kRxData + (q * 32 + lane) * 4,
+                       ((uint32_t)sha & 0xffffu) | ((uint32_t)shb << 16), rxfull_remote);
+        }
+        ++pi;
+        have = piece_next(a, end, W, pc);
       }
     } else {
       // ---- softmax of this CTA's rows ra = own_base + t/4, rb = ra + 8 ---------------
       // Thread t holds keys 8k + 2c, 8k + 2c + 1 (k = 0..7) of each 64-key tile.
       const int ra = own_base + (lane >> 2), rb = ra + 8;
-      const bool va = rt * BM + ra < nrows, vb = rt * BM + rb < nrows;
       const float sl2 = a.scale * 1.4426950408889634f;   // scores in log2 units
       const float* af = reinterpret_cast<const float*>(sm + OFF_AF);
       float* mref = reinterpret_cast<float*>(sm + OFF_MREF);
       float* lpart = reinterpret_cast<float*>(sm + OFF_LPART);
-      // Reference maxima last used by this warp and its row sums relative to them.
-      float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
       const int lead = 6 + 4 * par;               // the warp that re-arms this parity's receive barriers
 
-      if (nt > 0 && (a.flags & KDTV_FLAG_TEST_STALL))
+      if (G > 0 && (a.flags & KDTV_FLAG_TEST_STALL))
         alive = __all_sync(0xffffffffu, wait(BAR(B_STALL), 0, st, limit, W_STALL));
 
-      // This warp takes the tiles j = par, par + 2, ...; the running reference
-      // maxima pass between the two warps of the quadrant through shared memory.
+      // This warp takes the tiles g = par, par + 2, ... of the pair's sequence; the
+      // running reference maxima pass between the two warps of the quadrant
+      // through shared memory (restarting at -inf with every piece).
+      int g = 0, pi = 0;
       int next_rx = par;                          // first receive phase not yet consumed
       int next_af = par;
-      for (int j = par; alive && j < nt; j += 2) {
-        const int buf = j & 1;
-        alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (j >> 1) & 1, st, limit, W_S_FULL));
-        if (!alive) break;
+      // Writes O columns [col0, col0 + 32 nch32) of rows 32q .. 32q+31 of a piece
+      // (row tile rt, partial slot `slot`) once its P.V completed, then frees O.
+      auto write_o = [&](int slot, int rt, int phase, int col0, int nch32) -> bool {
+        if (!__all_sync(0xffffffffu, wait(BAR(B_O_FULL), phase, st, limit, W_O_FULL))) return false;
         tc_fence_after();
-        uint32_t v[32];                            // own partial scores (fp32)
-        tmem_ld_16x256b_x8(tmem + lane_own + kColS + 64 * buf, v);
-        tmem_wait_ld();
+        store_o_quadrant(tmem + (static_cast<uint32_t>(32 * q) << 16) + kColO + col0,
+                         a.part_o + ((long long)slot * BM + 32 * q) * a.d_c + rank * kHalf + col0, a.d_c,
+                         nrows - (rt * BM + 32 * q), nch32);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));   // QK^T of tile j+2 may overwrite
+        if (lane == 0) mbar_arrive(BAR(B_O_FREE));   // the next piece may overwrite O
+        return true;
+      };
+      while (alive && have) {
+        const bool va = pc.rt * BM + ra < nrows, vb = pc.rt * BM + rb < nrows;
+        const int L = pc.L, T = L + a.N;
+        const int k1 = min(T, pc.t1 * BN);
+        // Reference maxima last used by this warp and its row sums relative to them.
+        float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+        for (int j = pc.t0; j < pc.t1; ++j, ++g) {
+          if ((g & 1) != par) continue;
+          const int buf = g & 1;
+          alive = __all_sync(0xffffffffu, wait(BAR(B_S_FULL + buf), (g >> 1) & 1, st, limit, W_S_FULL));
+          if (!alive) break;
+          tc_fence_after();
+          uint32_t v[32];                          // own partial scores (fp32)
+          tmem_ld_16x256b_x8(tmem + lane_own + kColS + 64 * buf, v);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));   // QK^T of tile g+2 may overwrite
 
-        // + the peer's partial scores for our rows (its st.async filled rx[buf])
-        alive = __all_sync(0xffffffffu,
-                           wait<true>(BAR(B_RX_FULL + buf), (j >> 1) & 1, st, limit, W_RX_FULL));
-        if (!alive) break;
-        next_rx = j + 2;
-        if (warp == lead && lane == 0 && j + 2 < nt) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
-        float sa[16], sb[16];
-        {
-          const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
-          uint32_t pw[16], shw;
+          // + the peer's partial scores for our rows (its st.async filled rx[buf])
+          alive = __all_sync(0xffffffffu,
+                             wait<true>(BAR(B_RX_FULL + buf), (g >> 1) & 1, st, limit, W_RX_FULL));
+          if (!alive) break;
+          next_rx = g + 2;
+          if (warp == lead && lane == 0 && g + 2 < G) mbar_expect_tx(BAR(B_RX_FULL + buf), kRxBytes);
+          float sa[16], sb[16];
+          {
+            const uint32_t rxb = sbase + OFF_RX + buf * kRxStride;
+            uint32_t pw[16], shw;
 #pragma unroll
-          for (int m = 0; m < 4; ++m)
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(pw[4 * m]), "=r"(pw[4 * m + 1]), "=r"(pw[4 * m + 2]), "=r"(pw[4 * m + 3])
-                         : "r"(rxb + ((q * 4 + m) * 32 + lane) * 16) : "memory");
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(shw) : "r"(rxb + kRxData + (q * 32 + lane) * 4)
-                       : "memory");
-          const float pia = pow2f(-(int)(int16_t)(shw & 0xffffu));
-          const float pib = pow2f(-(int)(int16_t)(shw >> 16));
+            for (int m = 0; m < 4; ++m)
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(pw[4 * m]), "=r"(pw[4 * m + 1]), "=r"(pw[4 * m + 2]), "=r"(pw[4 * m + 3])
+                           : "r"(rxb + ((q * 4 + m) * 32 + lane) * 16) : "memory");
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(shw) : "r"(rxb + kRxData + (q * 32 + lane) * 4)
+                         : "memory");
+            const float pia = pow2f(-(int)(int16_t)(shw & 0xffffu));
+            const float pib = pow2f(-(int)(int16_t)(shw >> 16));
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pw[k]));
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pw[8 + k]));
-            sa[2 * k] = fmaf(fa.x, pia, __uint_as_float(v[4 * k]));
-            sa[2 * k + 1] = fmaf(fa.y, pia, __uint_as_float(v[4 * k + 1]));
-            sb[2 * k] = fmaf(fb.x, pib, __uint_as_float(v[4 * k + 2]));
-            sb[2 * k + 1] = fmaf(fb.y, pib, __uint_as_float(v[4 * k + 3]));
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));  // consumed
-
-        // visibility mask (only tiles that reach past the prefix, or rows past the end)
-        const int tb = k0 + j * BN;
-        if (!(va && vb && tb + BN <= L)) {
-#pragma unroll
-          for (int rsel = 0; rsel < 2; ++rsel) {
-            const bool vrow = rsel ? vb : va;
-            const int node = vrow ? (rt * BM + (rsel ? rb : ra)) / a.H : 0;
-            float* sv = rsel ? sb : sa;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int t = tb + 8 * (i >> 1) + 2 * c + (i & 1);
-              bool vis = false;
-              if (vrow && t < k1) {
-                if (t < L) {
-                  vis = true;
-                } else {
-                  const int jn = t - L;
-                  vis = (anc[4 * node + (jn >> 5)] >> (jn & 31)) & 1u;
-                }
-              }
-              if (!vis) sv[i] = -INFINITY;
+            for (int k = 0; k < 8; ++k) {
+              const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&pw[k]));
+              const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&pw[8 + k]));
+              sa[2 * k] = fmaf(fa.x, pia, __uint_as_float(v[4 * k]));
+              sa[2 * k + 1] = fmaf(fa.y, pia, __uint_as_float(v[4 * k + 1]));
+              sb[2 * k] = fmaf(fb.x, pib, __uint_as_float(v[4 * k + 2]));
+              sb[2 * k + 1] = fmaf(fb.y, pib, __uint_as_float(v[4 * k + 3]));
             }
           }
-        }
-        // row maxima: 16 keys per thread, then the row's four threads
-        float mta = max3f(sa[0], sa[1], sa[2]), mtb = max3f(sb[0], sb[1], sb[2]);
-#pragma unroll
-        for (int k = 3; k < 15; k += 2) {
-          mta = max3f(mta, sa[k], sa[k + 1]);
-          mtb = max3f(mtb, sb[k], sb[k + 1]);
-        }
-        mta = fmaxf(mta, sa[15]);
-        mtb = fmaxf(mtb, sb[15]);
-        mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 1));
-        mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 1));
-        mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 2)) * sl2;
-        mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 2)) * sl2;
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));  // consumed
 
-        // the reference maxima after tile j-1 (the other warp of this quadrant)
-        float mpa = -INFINITY, mpb = -INFINITY;
-        if (j >= 1) {
-          alive = __all_sync(0xffffffffu, wait(BAR(B_MREF + 4 * (par ^ 1) + q), ((j - 1) >> 1) & 1,
-                                               st, limit, W_MREF));
-          if (!alive) break;
-          mpa = mref[(par ^ 1) * BM + ra];
-          mpb = mref[(par ^ 1) * BM + rb];
-        }
-        // lazy rescale: move the reference max only when it grows by > 8 (log2);
-        // alpha rescales O (all tiles so far) to the new reference
-        float alpha_a = 1.f, alpha_b = 1.f;
-        float mna = mpa, mnb = mpb;
-        if (mta > mpa + 8.f) {
-          if (mpa != -INFINITY) alpha_a = ex2(mpa - mta);
-          mna = mta;
-        }
-        if (mtb > mpb + 8.f) {
-          if (mpb != -INFINITY) alpha_b = ex2(mpb - mtb);
-          mnb = mtb;
-        }
-        if (c == 0) {
-          mref[par * BM + ra] = mna;
-          mref[par * BM + rb] = mnb;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_MREF + 4 * par + q));
-        // this warp's row sums follow the reference
-        if (mna != m_a) {
-          if (m_a != -INFINITY) l_a *= ex2(m_a - mna);
-          m_a = mna;
-        }
-        if (mnb != m_b) {
-          if (m_b != -INFINITY) l_b *= ex2(m_b - mnb);
-          m_b = mnb;
-        }
-        // our rows' rescale factors -> the peer (it rescales its half of O)
-        {
-          const int afb = j & (kAfBufs - 1);
-          const uint32_t afr = mapa(BAR(B_AF_FULL + afb), peer);
-          if (c < 2)
-            st_async_u32(mapa(sbase + OFF_AF + (afb * BM + (c ? rb : ra)) * 4, peer),
-                         __float_as_uint(c ? alpha_b : alpha_a), afr);
-        }
-        const float nma = m_a == -INFINITY ? 0.f : -m_a, nmb = m_b == -INFINITY ? 0.f : -m_b;
-        uint32_t pa[8], pb[8];                     // bf16 pairs of P: keys 8k + 2c, +1
-        float psa = 0.f, psb = 0.f;
+          // visibility mask (only tiles that reach past the prefix, or rows past the end);
+          // each row's ancestor mask is one 16-byte load
+          const int tb = j * BN;
+          if (!(va && vb && tb + BN <= L)) {
+            const uint4* ag = reinterpret_cast<const uint4*>(a.anc_g) + (long long)pc.b * a.N;
+            const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 mka = va ? ag[(pc.rt * BM + ra) / a.H] : zero4;
+            const uint4 mkb = vb ? ag[(pc.rt * BM + rb) / a.H] : zero4;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          pa[k] = pack_bf16x2(ex2(fmaf(sa[2 * k], sl2, nma)), ex2(fmaf(sa[2 * k + 1], sl2, nma)));
-          pb[k] = pack_bf16x2(ex2(fmaf(sb[2 * k], sl2, nmb)), ex2(fmaf(sb[2 * k + 1], sl2, nmb)));
-          psa += __uint_as_float(pa[k] << 16) + __uint_as_float(pa[k] & 0xffff0000u);
-          psb += __uint_as_float(pb[k] << 16) + __uint_as_float(pb[k] & 0xffff0000u);
-        }
-        l_a += psa;
-        l_b += psb;
+            for (int rsel = 0; rsel < 2; ++rsel) {
+              const bool vrow = rsel ? vb : va;
+              const uint4 mk = rsel ? mkb : mka;
+              float* sv = rsel ? sb : sa;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int t = tb + 8 * (i >> 1) + 2 * c + (i & 1);
+                bool vis = false;
+                if (vrow && t < k1) {
+                  if (t < L) {
+                    vis = true;
+                  } else {
+                    const int jn = t - L;
+                    const int wsel = jn >> 5;
+                    const uint32_t w = wsel == 0 ? mk.x : (wsel == 1 ? mk.y : (wsel == 2 ? mk.z : mk.w));
+                    vis = (w >> (jn & 31)) & 1u;
+                  }
+                }
+                if (!vis) sv[i] = -INFINITY;
+              }
+            }
+          }
+          // row maxima: 16 keys per thread, then the row's four threads
+          float mta = max3f(sa[0], sa[1], sa[2]), mtb = max3f(sb[0], sb[1], sb[2]);
+#pragma unroll
+          for (int k = 3; k < 15; k += 2) {
+            mta = max3f(mta, sa[k], sa[k + 1]);
+            mtb = max3f(mtb, sb[k], sb[k + 1]);
+          }
+          mta = fmaxf(mta, sa[15]);
+          mtb = fmaxf(mtb, sb[15]);
+          mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 1));
+          mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 1));
+          mta = fmaxf(mta, __shfl_xor_sync(0xffffffffu, mta, 2)) * sl2;
+          mtb = fmaxf(mtb, __shfl_xor_sync(0xffffffffu, mtb, 2)) * sl2;
 
-        // P (single buffer) is free, and O stable, once P.V of tile j-1 completed in
-        // both CTAs (the (j-1)/2-th phase of the other parity's barrier)
-        if (j >= 1) {
-          alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + ((j - 1) & 1)), ((j - 1) >> 1) & 1, st,
-                                               limit, W_P_EMPTY));
-          if (!alive) break;
-        }
-        // P rows ra, rb: the pair for keys 8k + 2c is 4 bytes at offset 4c of the
-        // row's 16-byte chunk k, stored 128B-swizzled (chunk k of row r at k ^ (r & 7)).
-        {
-          const uint32_t prow_a = sbase + OFF_P + ra * 128 + 4 * c;
-          const uint32_t prow_b = sbase + OFF_P + rb * 128 + 4 * c;
+          // the reference maxima after tile g-1 (the other warp of this quadrant);
+          // its phase is consumed on every tile, the value only within a piece
+          float mpa = -INFINITY, mpb = -INFINITY;
+          pin(mta);
+          pin(mtb);
+          if (g >= 1) {
+            alive = __all_sync(0xffffffffu, wait(BAR(B_MREF + 4 * (par ^ 1) + q), ((g - 1) >> 1) & 1,
+                                                 st, limit, W_MREF));
+            if (!alive) break;
+            if (j > pc.t0) {
+              mpa = mref[(par ^ 1) * BM + ra];
+              mpb = mref[(par ^ 1) * BM + rb];
+            }
+          }
+          // lazy rescale: move the reference max only when it grows by > 8 (log2);
+          // alpha rescales O (all tiles so far) to the new reference
+          float alpha_a = 1.f, alpha_b = 1.f;
+          float mna = mpa, mnb = mpb;
+          if (mta > mpa + 8.f) {
+            if (mpa != -INFINITY) alpha_a = ex2(mpa - mta);
+            mna = mta;
+          }
+          if (mtb > mpb + 8.f) {
+            if (mpb != -INFINITY) alpha_b = ex2(mpb - mtb);
+            mnb = mtb;
+          }
+          if (c == 0) {
+            mref[par * BM + ra] = mna;
+            mref[par * BM + rb] = mnb;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_MREF + 4 * par + q));
+          // this warp's row sums follow the reference
+          if (mna != m_a) {
+            if (m_a != -INFINITY) l_a *= ex2(m_a - mna);
+            m_a = mna;
+          }
+          if (mnb != m_b) {
+            if (m_b != -INFINITY) l_b *= ex2(m_b - mnb);
+            m_b = mnb;
+          }
+          // our rows' rescale factors -> the peer (it rescales its half of O)
+          {
+            const int afb = g & (kAfBufs - 1);
+            const uint32_t afr = mapa(BAR(B_AF_FULL + afb), peer);
+            if (c < 2)
+              st_async_u32(mapa(sbase + OFF_AF + (afb * BM + (c ? rb : ra)) * 4, peer),
+                           __float_as_uint(c ? alpha_b : alpha_a), afr);
+          }
+          const float nma = m_a == -INFINITY ? 0.f : -m_a, nmb = m_b == -INFINITY ? 0.f : -m_b;
+          uint32_t pa[8], pb[8];                   // bf16 pairs of P: keys 8k + 2c, +1
+          float psa = 0.f, psb = 0.f;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            asm volatile("st.shared.b32 [%0], %1;" :: "r"(prow_a + ((k ^ (ra & 7)) << 4)), "r"(pa[k]) : "memory");
-            asm volatile("st.shared.b32 [%0], %1;" :: "r"(prow_b + ((k ^ (rb & 7)) << 4)), "r"(pb[k]) : "memory");
+            pa[k] = pack_bf16x2(ex2(fmaf(sa[2 * k], sl2, nma)), ex2(fmaf(sa[2 * k + 1], sl2, nma)));
+            pb[k] = pack_bf16x2(ex2(fmaf(sb[2 * k], sl2, nmb)), ex2(fmaf(sb[2 * k + 1], sl2, nmb)));
+            psa += __uint_as_float(pa[k] << 16) + __uint_as_float(pa[k] & 0xffff0000u);
+            psb += __uint_as_float(pb[k] << 16) + __uint_as_float(pb[k] & 0xffff0000u);
           }
+          l_a += psa;
+          l_b += psb;
+
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            pin(pa[k]);
+            pin(pb[k]);
+          }
+          pin(l_a);
+          pin(l_b);
+          // P (single buffer) is free, and O stable, once P.V of tile g-1 completed in
+          // both CTAs (the (g-1)/2-th phase of the other parity's barrier)
+          if (g >= 1) {
+            alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + ((g - 1) & 1)), ((g - 1) >> 1) & 1, st,
+                                                 limit, W_P_EMPTY));
+            if (!alive) break;
+          }
+          // P rows ra, rb: the pair for keys 8k + 2c is 4 bytes at offset 4c of the
+          // row's 16-byte chunk k, stored 128B-swizzled (chunk k of row r at k ^ (r & 7)).
+          {
+            const uint32_t prow_a = sbase + OFF_P + ra * 128 + 4 * c;
+            const uint32_t prow_b = sbase + OFF_P + rb * 128 + 4 * c;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              asm volatile("st.shared.b32 [%0], %1;" :: "r"(prow_a + ((k ^ (ra & 7)) << 4)), "r"(pa[k]) : "memory");
+              asm volatile("st.shared.b32 [%0], %1;" :: "r"(prow_b + ((k ^ (rb & 7)) << 4)), "r"(pb[k]) : "memory");
+            }
+          }
+          fence_async_smem();                       // visible to the tensor core and the copy engine
+          __syncwarp();
+          if (lane == 0) {
+            // our 16 rows of this quadrant are one contiguous 2 KiB block
+            const uint32_t off = OFF_P + own_base * 128;
+            bulk_copy_to_peer(mapa(sbase + off, peer), sbase + off, kPQuadBytes,
+                              mapa(BAR(B_P_RX), peer));
+          }
+          // the peer's rescale factors for its rows of this quadrant: both halves of
+          // O must carry the same reference maxima before P.V of this tile
+          const int afb = g & (kAfBufs - 1);
+          alive = __all_sync(0xffffffffu,
+                             wait<true>(BAR(B_AF_FULL + afb), (g / kAfBufs) & 1, st, limit, W_AF));
+          if (!alive) break;
+          next_af = g + 2;
+          const float qa = af[afb * BM + (ra ^ 16)], qb = af[afb * BM + (rb ^ 16)];
+          if (warp == lead && lane == 0 && g + kAfBufs < G)
+            mbar_expect_tx(BAR(B_AF_FULL + afb), kAfBytes);
+          if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f || qa != 1.f || qb != 1.f)) {
+            tc_fence_after();
+            rescale_o_rows(tmem + lane_own + kColO, alpha_a, alpha_b);
+            rescale_o_rows(tmem + lane_peer + kColO, qa, qb);
+            tmem_wait_st();
+            tc_fence_before();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_P_FULL));
         }
-        fence_async_smem();                         // visible to the tensor core and the copy engine
-        __syncwarp();
-        if (lane == 0) {
-          // our 16 rows of this quadrant are one contiguous 2 KiB block
-          const uint32_t off = OFF_P + own_base * 128;
-          bulk_copy_to_peer(mapa(sbase + off, peer), sbase + off, kPQuadBytes,
-                            mapa(BAR(B_P_RX), peer));
-        }
-        // the peer's rescale factors for its rows of this quadrant: both halves of
-        // O must carry the same reference maxima before P.V of this tile
-        const int afb = j & (kAfBufs - 1);
-        alive = __all_sync(0xffffffffu,
-                           wait<true>(BAR(B_AF_FULL + afb), (j / kAfBufs) & 1, st, limit, W_AF));
         if (!alive) break;
-        next_af = j + 2;
-        const float qa = af[afb * BM + (ra ^ 16)], qb = af[afb * BM + (rb ^ 16)];
-        if (warp == lead && lane == 0 && j + kAfBufs < nt)
-          mbar_expect_tx(BAR(B_AF_FULL + afb), kAfBytes);
-        if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f || qa != 1.f || qb != 1.f)) {
-          tc_fence_after();
-          rescale_o_rows(tmem + lane_own + kColO, alpha_a, alpha_b);
-          rescale_o_rows(tmem + lane_peer + kColO, qa, qb);
-          tmem_wait_st();
-          tc_fence_before();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_P_FULL));
-      }
 
-      // After an abort, let what the peer may still be sending land before exit
-      // (receive phases that were armed but not consumed); bounded, errors ignored.
-      if (!alive) {
-        if (next_rx < nt) drain_wait(BAR(B_RX_FULL + (next_rx & 1)), (next_rx >> 1) & 1, 200000ull);
-        for (int t = next_af; t < next_af + kAfBufs && t < nt; t += 2)
-          drain_wait(BAR(B_AF_FULL + (t & (kAfBufs - 1))), (t / kAfBufs) & 1, 200000ull);
-      }
-
-      // (m, l) of our rows: row sums meet across the row's four threads
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-      l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-      l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-      // the odd-tile warp hands its (m, l) to the even-tile warp, which merges
-      // them (the later reference is the larger) and writes the row's (m, l)
-      if (par == 1) {
-        if (c == 0) {
-          lpart[ra] = m_a; lpart[BM + ra] = l_a;
-          lpart[rb] = m_b; lpart[BM + rb] = l_b;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_LSUM));
-      } else if (ok) {
-        alive = __all_sync(0xffffffffu, wait(BAR(B_LSUM), 0, st, limit, W_LSUM)) && alive;
-        if (alive) {
+        // ---- end of the piece: (m, l) of our rows and the unnormalised o_lat half -------
+        // Row sums meet across the row's four threads; the odd-tile warp hands its
+        // (m, l) to the even-tile warp, which merges them (the later reference is
+        // the larger) and writes the row's (m, l) to the piece's slot.
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+        l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+        l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+        if (par == 1) {
+          // the even-tile warps have read the previous piece's hand-over
+          if (pi >= 1) {
+            alive = __all_sync(0xffffffffu, wait(BAR(B_L_FREE), (pi - 1) & 1, st, limit, W_LSUM));
+            if (!alive) break;
+          }
+          if (c == 0) {
+            lpart[ra] = m_a; lpart[BM + ra] = l_a;
+            lpart[rb] = m_b; lpart[BM + rb] = l_b;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_LSUM));
+        } else {
+          alive = __all_sync(0xffffffffu, wait(BAR(B_LSUM), pi & 1, st, limit, W_LSUM));
+          if (!alive) break;
           const float m1a = lpart[ra], l1a = lpart[BM + ra], m1b = lpart[rb], l1b = lpart[BM + rb];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(B_L_FREE));
           const float ma = fmaxf(m_a, m1a), mb = fmaxf(m_b, m1b);
           l_a = (m_a == -INFINITY ? 0.f : l_a * ex2(m_a - ma)) + (m1a == -INFINITY ? 0.f : l1a * ex2(m1a - ma));
           l_b = (m_b == -INFINITY ? 0.f : l_b * ex2(m_b - mb)) + (m1b == -INFINITY ? 0.f : l1b * ex2(m1b - mb));
           m_a = ma;
           m_b = mb;
-        }
-      }
-      if (ok && alive && c == 0 && par == 0) {
-        const long long rows = (long long)a.B * a.N * a.H;
+          if (c == 0) {
 #pragma unroll
-        for (int rsel = 0; rsel < 2; ++rsel) {
-          const bool vrow = rsel ? vb : va;
-          const float l = rsel ? l_b : l_a, m = rsel ? m_b : m_a;
-          if (vrow) {
-            float* ml = a.part_ml + ((long long)s * rows + req_row0 + rt * BM + (rsel ? rb : ra)) * 2;
-            const bool has = nt > 0 && l > 0.f;
-            ml[0] = has ? m * 0.6931471805599453f : -INFINITY;
-            ml[1] = has ? l : 0.f;
+            for (int rsel = 0; rsel < 2; ++rsel) {
+              if (rsel ? vb : va) {
+                const float l = rsel ? l_b : l_a, m = rsel ? m_b : m_a;
+                float* ml = a.part_ml + ((long long)pc.slot * BM + (rsel ? rb : ra)) * 2;
+                ml[0] = l > 0.f ? m * 0.6931471805599453f : -INFINITY;
+                ml[1] = l > 0.f ? l : 0.f;
+              }
+            }
           }
         }
-      }
-    }
-
-    // ---- epilogue: unnormalised partial o_lat half of rows 32q .. 32q+31 ----------------
-    // (.32x32b: thread = row; the sender warp writes O columns 0..127, the softmax 128..255)
-    if (alive && nt > 0 && par == 0)
-      alive = __all_sync(0xffffffffu, wait(BAR(B_O_FULL), 0, st, limit, W_O_FULL));
-    const int r = 32 * q + lane;
-    const int rr = rt * BM + r;
-    if (ok && alive && nt > 0 && par == 0) {
-      const long long rows = (long long)a.B * a.N * a.H;
-      const int g = is_softmax ? 1 : 0;
-      float* po = a.part_o + ((long long)s * rows + req_row0 + (rr < nrows ? rr : 0)) * a.d_c +
-                  rank * kHalf + 128 * g;
-      tc_fence_after();
-      for (int cc = 0; cc < 4; ++cc) {
-        float ov[32];
-        tmem_ld32(tmem + lane32 + kColO + 128 * g + 32 * cc, ov);
-        tmem_wait_ld();
-        if (rr < nrows) {
-#pragma unroll
-          for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(po + 32 * cc + k) =
-                make_float4(ov[k], ov[k + 1], ov[k + 2], ov[k + 3]);
+        // O write-out.  After the pair's last piece the 8 softmax warps write 128
+        // columns each.  When another piece follows, the 4 warps that took this
+        // piece's last tile write all 256 columns while the other 4 go on with
+        // the next piece's first tile (B_O_FREE counts 4 arrivals).
+        Piece nx = pc;
+        have = piece_next(a, end, W, nx);
+        if (!have ? !write_o(pc.slot, pc.rt, pi & 1, 128 * par, 4)
+                  : (((g - 1) & 1) == par && !write_o(pc.slot, pc.rt, pi & 1, 0, 8))) {
+          alive = false;
+          break;
         }
+        ++pi;
+        pc = nx;
+      }
+
+      // After an abort, let what the peer may still be sending land before exit
+      // (receive phases that were armed but not consumed); bounded, errors ignored.
+      if (!alive) {
+        if (next_rx < G) drain_wait(BAR(B_RX_FULL + (next_rx & 1)), (next_rx >> 1) & 1, 200000ull);
+        for (int t = next_af; t < next_af + kAfBufs && t < G; t += 2)
+          drain_wait(BAR(B_AF_FULL + (t & (kAfBufs - 1))), (t / kAfBufs) & 1, 200000ull);
       }
     }
   }
@@ -772,7 +933,80 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
   cluster_sync();   // the peer may still arrive on our barriers until here
 }
 
-int row_tiles_of(const kdtv_dims* d) { return (d->N * d->H + BM - 1) / BM; }
+// ---- plan kernel ----------------------------------------------------------------------
+// CTA b < B: the ancestor masks of request b (and the tree check).  CTA B: the
+// stream-K plan.  Request b contributes rt_count row tiles of u_b = ceil((L_b
+// + N) / 64) key tiles each (0 if its prefix length is invalid); row tile r
+// starts at unit S_r of the whole sequence.  With U units in all, W =
+// max(ceil(U / clusters), wmin), or the forced W.  A row tile is cut where a
+// multiple of W falls inside it; its pieces take the consecutive partial slots
+// from base_r = r + floor(S_r / W) (base_{r+1} - base_r = 1 + the multiples of
+// W in (S_r, S_{r+1}], so the ranges never overlap).
+__global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
+  grid_dep_launch();   // the absorb kernel does not read the plan
+  const int tid = threadIdx.x;
+  if ((int)blockIdx.x < a.B) {
+    const int b = blockIdx.x;
+    __shared__ int32_t par_s[kMaxNodes];
+    if (tid < a.N) par_s[tid] = a.parent[(long long)b * a.N + tid];
+    __syncthreads();
+    if (tid < a.N) {
+      uint32_t m[4];
+      ancestor_mask_smem(a, b, par_s, tid, m);
+      reinterpret_cast<uint4*>(a.anc_g)[(long long)b * a.N + tid] = make_uint4(m[0], m[1], m[2], m[3]);
+    }
+    return;
+  }
+  __shared__ int tmp[256];
+  __shared__ int carry;
+  const int R = a.B * a.rt_count;
+  int* e = a.sk + kSkHeader;
+  const int cap = a.page_size ? a.max_pages * a.page_size : a.t_stride;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int r0 = 0; r0 < R; r0 += 256) {
+    const int r = r0 + tid;
+    int u = 0;
+    if (r < R) {
+      const int b = r / a.rt_count;
+      const int L = a.prefix_len[b];
+      const bool ok = L >= 0 && (long long)L + a.N <= cap;
+      if (!ok && r % a.rt_count == 0) record_error(a.status, KDTV_ERR_BAD_PREFIX, (unsigned)b);
+      u = ok ? (L + a.N + BN - 1) / BN : 0;
+    }
+    tmp[tid] = u;
+    __syncthreads();
+    for (int o = 1; o < 256; o <<= 1) {     // inclusive scan
+      const int x = tid >= o ? tmp[tid - o] : 0;
+      __syncthreads();
+      tmp[tid] += x;
+      __syncthreads();
+    }
+    if (r < R) {
+      e[3 * r] = carry + tmp[tid] - u;
+      e[3 * r + 1] = u;
+    }
+    __syncthreads();
+    if (tid == 255) carry += tmp[255];
+    __syncthreads();
+  }
+  const int U = carry;
+  int W;
+  if (a.sk_wforce > 0) {
+    W = a.sk_wforce > a.sk_wmin ? a.sk_wforce : a.sk_wmin;
+  } else {
+    W = (U + a.sk_clusters - 1) / a.sk_clusters;
+    if (W < a.sk_wmin) W = a.sk_wmin;
+  }
+  if (W < 1) W = 1;
+  for (int r = tid; r < R; r += 256) e[3 * r + 2] = r + e[3 * r] / W;
+  if (tid == 0) {
+    a.sk[0] = U;
+    a.sk[1] = W;
+    a.sk[2] = a.sk_clusters;
+    a.sk[3] = R;
+  }
+}
 
 }  // namespace
 
@@ -821,29 +1055,15 @@ int tc_supported(const kdtv_dims* d) {
   return 1;
 }
 
-int tc_launches(const kdtv_dims* d, int splits) {
-  if (d->flags & KDTV_FLAG_SIMT_PROJ) return 4;
+int tc_launches(const kdtv_dims* d, int /*splits*/) {
+  // plan, absorb, attention, then the fused combine + up-projection (or the
+  // fp32 combine and up-projection kernels)
+  if (d->flags & KDTV_FLAG_SIMT_PROJ) return 5;
   Args a;
-  a.dtype = d->dtype; a.d_c = d->d_c; a.d_v = d->d_v; a.d_nope = d->d_nope; a.splits = splits;
-  return 2 + (combine_uproj_tc_ok(a) ? 1 : 2);
-}
-
-// Split-KV chunk: pick the split count s that minimises the modelled
-// makespan  ceil(2 * items(s) / SMs) / s  (two CTAs per item, one CTA per
-// SM), with a small per-split cost for the partials it writes and merges.
-int tc_chunk(const kdtv_dims* d, int sms) {
-  const long long base = (long long)d->B * row_tiles_of(d);
-  const int t_cap = d->page_size ? d->max_pages * d->page_size : d->t_stride;
-  const int max_s = (t_cap + 511) / 512;
-  int best_s = 1;
-  double best = 1e30;
-  for (int s = 1; s <= (max_s < 64 ? max_s : 64); ++s) {
-    const double waves = (double)((2 * base * s + sms - 1) / sms);
-    const double cost = waves / s + 0.02 * s;
-    if (cost < best - 1e-9) { best = cost; best_s = s; }
-  }
-  int chunk = (t_cap + best_s - 1) / best_s;
-  return (chunk + BN - 1) / BN * BN;
+  a.dtype = d->dtype; a.d_c = d->d_c; a.d_v = d->d_v; a.d_nope = d->d_nope; a.splits = 1;
+  int dummy = 0;
+  a.sk = &dummy;
+  return 3 + (combine_uproj_tc_ok(a) ? 1 : 2);
 }
 
 cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t* ev) {
@@ -859,21 +1079,25 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
     return cudaErrorInvalidValue;
 
   const bool simt_proj = a.flags & KDTV_FLAG_SIMT_PROJ;
-  cudaError_t e = simt_proj ? launch_absorb(a, st, /*bf16_out=*/true) : launch_absorb_tc(a, st);
+  if (a.N > kMaxNodes || !a.sk || !a.anc_g || a.sk_clusters < 1) return cudaErrorInvalidValue;
+  // The plan runs beside the absorb kernel (which waits for it before it
+  // exits), so the attention kernel sees both once the absorb has completed.
+  sk_plan_kernel<<<a.B + 1, 256, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = simt_proj ? launch_absorb(a, st, /*bf16_out=*/true)
+                : launch_absorb_tc(a, st, /*after_plan=*/ev == nullptr);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[1], st);
 
   TcCfg cfg;
-  cfg.row_tiles = (a.N * a.H + BM - 1) / BM;
   cfg.limit_ns = (a.flags & KDTV_FLAG_TEST_STALL) ? 20000000ull : 2000000000ull;
-  const long long items = (long long)a.B * cfg.row_tiles * a.splits;
-  if (2 * items > 0x7fffffffll) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
   if (e != cudaSuccess) return e;
   // Overlap with the absorb kernel's tail unless phase events split the call.
-  e = launch_ex(attn_tc_kernel, dim3((unsigned)(2 * items)), dim3(kThreads), kSmemBytes, st,
-                /*pdl=*/ev == nullptr && !simt_proj, tqr, tck, tkr, a, cfg);
+  e = launch_ex(attn_tc_kernel, dim3((unsigned)(2 * a.sk_clusters)), dim3(kThreads), kSmemBytes,
+                st, /*pdl=*/ev == nullptr && !simt_proj, tqr, tck, tkr, a, cfg);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], st);
   return simt_proj ? launch_combine_uproj(a, p, st, ev) : launch_combine_uproj_tc(a, p, st, ev);

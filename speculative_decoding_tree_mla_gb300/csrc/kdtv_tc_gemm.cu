@@ -120,6 +120,9 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   tc_fence_before();
   __syncthreads();
   if (warp == 0) { tc_fence_after(); tmem_dealloc(tmem, AB_NR); }
+  // Launched beside the attention plan: this grid completes only after the
+  // plan has, so the attention kernel's wait on it covers both.
+  grid_dep_wait();
 }
 
 // ---- A5 + A6: split combine fused with the W_UV up-projection -------------------------
@@ -130,7 +133,8 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 constexpr int UP_MAX_SPLITS = 64;
 constexpr int UP_OFF_B = 8 * 128 * 128;
 __host__ __device__ constexpr int up_off_w(int nr) { return UP_OFF_B + 8 * nr * 128; }
-__host__ __device__ constexpr int up_off_bar(int nr) { return up_off_w(nr) + nr * UP_MAX_SPLITS * 4; }
+__host__ __device__ constexpr int up_off_pr(int nr) { return up_off_w(nr) + nr * UP_MAX_SPLITS * 4; }
+__host__ __device__ constexpr int up_off_bar(int nr) { return up_off_pr(nr) + nr * 16 + 16; }
 __host__ __device__ constexpr int up_smem(int nr) { return up_off_bar(nr) + 64 + 1024; }
 __host__ __device__ constexpr int up_tmem_cols(int nr) { return nr < 32 ? 32 : nr; }
 
@@ -140,7 +144,7 @@ constexpr int UP_BATCH = 4;       // row/8-column units merged per thread per pa
 template <int UP_NR>
 __global__ void __launch_bounds__(UP_THREADS, 1)
 combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) {
-  constexpr int UP_OFF_W = up_off_w(UP_NR), UP_OFF_BAR = up_off_bar(UP_NR);
+  constexpr int UP_OFF_W = up_off_w(UP_NR), UP_OFF_PR = up_off_pr(UP_NR), UP_OFF_BAR = up_off_bar(UP_NR);
   constexpr int kCols = up_tmem_cols(UP_NR);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -151,9 +155,11 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   const int r0 = blockIdx.y * UP_NR;
   const int BNr = a.B * a.N;
   const int nr = min(UP_NR, BNr - r0);
-  const int S = a.splits;
-  const long long rows = (long long)BNr * a.H;
   float* wts = reinterpret_cast<float*>(sm + UP_OFF_W);
+  // per row: partial row index of its partial s = pr_base[r] + s * pr_step[r]
+  long long* pr_base = reinterpret_cast<long long*>(sm + UP_OFF_PR);
+  int* pr_step = reinterpret_cast<int*>(sm + UP_OFF_PR + UP_NR * 8);
+  int* s_max = reinterpret_cast<int*>(sm + UP_OFF_PR + UP_NR * 12);
   const uint32_t bar_full = sbase + UP_OFF_BAR, bar_mma = bar_full + 8;
   volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + UP_OFF_BAR + 16);
 
@@ -175,31 +181,39 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
 
   grid_dep_wait();   // the split partials are written by the attention kernel
 
-  // Split weights per row, with 1 / sum_s e^{m_s - m*} l_s folded in.
+  // Partial weights per row, with 1 / sum_s e^{m_s - m*} l_s folded in.
+  if (tid == 0) *s_max = 0;
+  __syncthreads();
   if (tid < UP_NR) {
     const int r = tid;
     float* w = wts + r * UP_MAX_SPLITS;
+    for (int s = 0; s < UP_MAX_SPLITS; ++s) w[s] = 0.f;
+    pr_base[r] = 0;
+    pr_step[r] = 0;
     if (r < nr) {
-      const long long grow = (long long)(r0 + r) * a.H + h;
+      const PartialRef pr = partials_of_row(a, (long long)(r0 + r) * a.H + h);
+      const int S = pr.count < UP_MAX_SPLITS ? pr.count : UP_MAX_SPLITS;
+      pr_base[r] = pr.base;
+      pr_step[r] = (int)pr.step;
       float m = -INFINITY;
       for (int s = 0; s < S; ++s) {
-        const float* ml = a.part_ml + ((long long)s * rows + grow) * 2;
+        const float* ml = a.part_ml + (pr.base + s * pr.step) * 2;
         if (ml[1] > 0.f) m = fmaxf(m, ml[0]);
       }
       float l = 0.f;
       for (int s = 0; s < S; ++s) {
-        const float* ml = a.part_ml + ((long long)s * rows + grow) * 2;
+        const float* ml = a.part_ml + (pr.base + s * pr.step) * 2;
         const float e = ml[1] > 0.f ? expf(ml[0] - m) : 0.f;
         w[s] = e;
         l += e * ml[1];
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       for (int s = 0; s < S; ++s) w[s] *= inv;
-    } else {
-      for (int s = 0; s < S; ++s) w[s] = 0.f;
+      atomicMax(s_max, S);
     }
   }
   __syncthreads();
+  const int S = *s_max;
 
   // o_lat rows -> bf16, 128-byte swizzled K-major operand: row r, 8-column unit u.
   // Each pass merges UP_BATCH units per thread with all their loads in flight.
@@ -223,7 +237,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
           ws[q][uu] = (s < S && idx < UP_NR * 64 && r < nr) ? wts[r * UP_MAX_SPLITS + s] : 0.f;
           if (ws[q][uu] != 0.f) {
             const float4* src = reinterpret_cast<const float4*>(
-                a.part_o + ((long long)s * rows + (long long)(r0 + r) * a.H + h) * 512 + 8 * u);
+                a.part_o + (pr_base[r] + (long long)s * pr_step[r]) * 512 + 8 * u);
             x[q][uu][0] = src[0];
             x[q][uu][1] = src[1];
           } else {
@@ -307,10 +321,11 @@ bool absorb_tc_ok(const Args& a) {
 }
 
 bool combine_uproj_tc_ok(const Args& a) {
-  return a.dtype == KDTV_BF16 && a.d_c == 512 && a.d_v == 128 && a.splits <= UP_MAX_SPLITS;
+  return a.dtype == KDTV_BF16 && a.d_c == 512 && a.d_v == 128 &&
+         (a.sk != nullptr || a.splits <= UP_MAX_SPLITS);
 }
 
-cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st) {
+cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st, bool after_plan) {
   if (!absorb_tc_ok(a)) return launch_absorb(a, st, /*bf16_out=*/true);
   CUtensorMap tw, tq;
   const uint64_t BNr = (uint64_t)a.B * a.N;
@@ -322,8 +337,7 @@ cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(512 / AB_M, a.H, (unsigned)((BNr + AB_NR - 1) / AB_NR));
-  absorb_tc_kernel<<<grid, kThreads, smem, st>>>(tw, tq, a);
-  return cudaGetLastError();
+  return launch_ex(absorb_tc_kernel, grid, dim3(kThreads), smem, st, after_plan, tw, tq, a);
 }
 
 namespace {
