@@ -88,7 +88,7 @@ int make_plan(const kdtv_dims* d, Plan* p) {
     p->off_part_o = off;  off = align256(off + (size_t)p->slots * 128 * d->d_c * sizeof(float));
     p->off_part_ml = off; off = align256(off + (size_t)p->slots * 128 * 2 * sizeof(float));
     p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
-    p->off_sk = off;      off = align256(off + (size_t)(kSkHeader + 3 * R) * sizeof(int));
+    p->off_sk = off;      off = align256(off + (size_t)(kSkHeader + 3 * R + clusters) * sizeof(int));
     p->off_anc = off;     off = align256(off + (size_t)d->B * d->N * 4 * sizeof(uint32_t));
   } else {
     p->heads_per_cta = d->H < 16 ? d->H : 16;

@@ -71,7 +71,8 @@ struct Args {
   float* part_ml;         // [splits, rows, 2] or [slots, 128, 2]  (running max m, sum l)
   float* o_lat;           // [rows, d_c]
   // Stream-K plan of the tensor-core attention (nullptr: split layout).
-  int* sk;                // kSkHeader ints {U, W, clusters, R}, then {S_r, u_r, base_r} per row tile
+  int* sk;                // kSkHeader ints {U, W, clusters, R}, then {S_r, u_r, base_r} per row tile,
+                          // then the row tile of each CTA pair's first unit
   uint32_t* anc_g;        // [B, N, 4] ancestor masks, written by the plan kernel
   int rt_count;           // 128-row tiles per request
   int sk_clusters;        // CTA pairs launched

@@ -162,18 +162,13 @@ __device__ __forceinline__ void piece_fill(const Args& a, int r, int beg, int en
   p.L = a.prefix_len[p.b];
 }
 
-// First piece of the unit range [beg, end); false if the range is empty.
-__device__ bool piece_first(const Args& a, int beg, int end, int W, Piece& p) {
+// First piece of CTA pair cl (unit range [beg, end)); false if the range is
+// empty.  The plan lists the row tile holding each pair's first unit.
+__device__ bool piece_first(const Args& a, int cl, int beg, int end, int W, Piece& p) {
   if (beg >= end) return false;
   const int R = a.sk[3];
-  int lo = 0, hi = R - 1;                     // last row tile starting at or before beg
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (sk_row(a, mid)[0] <= beg) lo = mid; else hi = mid - 1;
-  }
-  int r = lo;
-  while (r < R && sk_row(a, r)[0] + sk_row(a, r)[1] <= beg) ++r;
-  if (r >= R) return false;
+  const int r = a.sk[kSkHeader + 3 * R + cl];
+  if (r < 0 || r >= R) return false;
   piece_fill(a, r, beg, end, W, p);
   return true;
 }
@@ -377,7 +372,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         if (rank == 0) tma_prefetch_2d(&tm_krope, 0, row);
       };
       Piece pc;
-      bool have = piece_first(a, beg, end, W, pc);
+      bool have = piece_first(a, cl, beg, end, W, pc);
       int g = 0, pi = 0, issued = 0, qr_issued = 0;
       bool alive = true;
       while (alive && have) {
@@ -421,7 +416,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     if (lane == 0 && G > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, 0, 0);
       Piece pc;
-      bool have = piece_first(a, beg, end, W, pc);
+      bool have = piece_first(a, cl, beg, end, W, pc);
       int g = 0, pi = 0;
       bool alive = true;
       while (alive && have) {
@@ -467,7 +462,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     if (lane == 0 && G > 0) {
       constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
       Piece pc;
-      bool have = piece_first(a, beg, end, W, pc);
+      bool have = piece_first(a, cl, beg, end, W, pc);
       int g = 0, pi = 0, p_armed = 1;              // phases of B_P_RX armed so far
       bool alive = true;
       while (alive && have) {
@@ -521,7 +516,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     const uint32_t lane32 = static_cast<uint32_t>(32 * q) << 16;
     bool alive = true;
     Piece pc;
-    bool have = piece_first(a, beg, end, W, pc);
+    bool have = piece_first(a, cl, beg, end, W, pc);
 
     if (!is_softmax) {
       // ---- sender: each piece's Q into TMEM; the peer's score rows -> its receive buffer --
@@ -941,7 +936,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
 // max(ceil(U / clusters), wmin), or the forced W.  A row tile is cut where a
 // multiple of W falls inside it; its pieces take the consecutive partial slots
 // from base_r = r + floor(S_r / W) (base_{r+1} - base_r = 1 + the multiples of
-// W in (S_r, S_{r+1}], so the ranges never overlap).
+// W in (S_r, S_{r+1}], so the ranges never overlap).  The plan also lists, for
+// each CTA pair c, the row tile that holds its first unit c W.
 __global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
   grid_dep_launch();   // the absorb kernel does not read the plan
   const int tid = threadIdx.x;
@@ -999,7 +995,17 @@ __global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
     if (W < a.sk_wmin) W = a.sk_wmin;
   }
   if (W < 1) W = 1;
-  for (int r = tid; r < R; r += 256) e[3 * r + 2] = r + e[3 * r] / W;
+  // partial slots, and the row tile holding the first unit c W of each pair c
+  int* first = e + 3 * R;
+  const int npair = a.sk_clusters;
+  for (int c = tid; c < npair; c += 256) first[c] = R;
+  __syncthreads();
+  for (int r = tid; r < R; r += 256) {
+    const int S = e[3 * r], u = e[3 * r + 1];
+    e[3 * r + 2] = r + S / W;
+    const long long c_end = ((long long)S + u + W - 1) / W;
+    for (long long c = ((long long)S + W - 1) / W; c < c_end && c < npair; ++c) first[c] = r;
+  }
   if (tid == 0) {
     a.sk[0] = U;
     a.sk[1] = W;

@@ -181,36 +181,55 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
 
   grid_dep_wait();   // the split partials are written by the attention kernel
 
-  // Partial weights per row, with 1 / sum_s e^{m_s - m*} l_s folded in.
+  // Partial weights per row, with 1 / sum_s e^{m_s - m*} l_s folded in.  The
+  // UP_THREADS / UP_NR threads of a row (adjacent lanes) take every
+  // (UP_THREADS / UP_NR)-th partial and meet by shuffles, so the (m, l) loads
+  // of a row are in flight together.
+  constexpr int kTpr = UP_THREADS / UP_NR;
+  static_assert(kTpr >= 2 && kTpr <= 32 && (kTpr & (kTpr - 1)) == 0, "threads per row");
   if (tid == 0) *s_max = 0;
+  for (int i = tid; i < UP_NR * UP_MAX_SPLITS; i += UP_THREADS) wts[i] = 0.f;
   __syncthreads();
-  if (tid < UP_NR) {
-    const int r = tid;
-    float* w = wts + r * UP_MAX_SPLITS;
-    for (int s = 0; s < UP_MAX_SPLITS; ++s) w[s] = 0.f;
-    pr_base[r] = 0;
-    pr_step[r] = 0;
-    if (r < nr) {
-      const PartialRef pr = partials_of_row(a, (long long)(r0 + r) * a.H + h);
-      const int S = pr.count < UP_MAX_SPLITS ? pr.count : UP_MAX_SPLITS;
-      pr_base[r] = pr.base;
-      pr_step[r] = (int)pr.step;
-      float m = -INFINITY;
-      for (int s = 0; s < S; ++s) {
-        const float* ml = a.part_ml + (pr.base + s * pr.step) * 2;
-        if (ml[1] > 0.f) m = fmaxf(m, ml[0]);
-      }
-      float l = 0.f;
-      for (int s = 0; s < S; ++s) {
-        const float* ml = a.part_ml + (pr.base + s * pr.step) * 2;
-        const float e = ml[1] > 0.f ? expf(ml[0] - m) : 0.f;
-        w[s] = e;
-        l += e * ml[1];
-      }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      for (int s = 0; s < S; ++s) w[s] *= inv;
-      atomicMax(s_max, S);
+  {
+    const int r = tid / kTpr, sub = tid % kTpr;
+    const bool live = r < nr;
+    const PartialRef pr = partials_of_row(a, (long long)(r0 + (live ? r : 0)) * a.H + h);
+    const int S = live ? (pr.count < UP_MAX_SPLITS ? pr.count : UP_MAX_SPLITS) : 0;
+    if (sub == 0) {
+      pr_base[r] = live ? pr.base : 0;
+      pr_step[r] = live ? (int)pr.step : 0;
     }
+    constexpr int kPer = UP_MAX_SPLITS / kTpr;        // partials per thread at most
+    float2 ml[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int s = sub + k * kTpr;
+      ml[k] = s < S ? *reinterpret_cast<const float2*>(a.part_ml + (pr.base + (long long)s * pr.step) * 2)
+                    : make_float2(-INFINITY, 0.f);
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (ml[k].y > 0.f) m = fmaxf(m, ml[k].x);
+#pragma unroll
+    for (int o = 1; o < kTpr; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const float e = ml[k].y > 0.f ? expf(ml[k].x - m) : 0.f;
+      ml[k].x = e;
+      l += e * ml[k].y;
+    }
+#pragma unroll
+    for (int o = 1; o < kTpr; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float* w = wts + r * UP_MAX_SPLITS;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int s = sub + k * kTpr;
+      if (s < S) w[s] = ml[k].x * inv;
+    }
+    if (live && sub == 0) atomicMax(s_max, S);
   }
   __syncthreads();
   const int S = *s_max;
