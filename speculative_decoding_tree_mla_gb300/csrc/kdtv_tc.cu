@@ -67,11 +67,13 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 64;           // keys per tile (MMA N of Q.K^T)
 constexpr int CH = 64;           // bf16 columns per 128-byte swizzled chunk
 constexpr int kHalf = 256;       // latent columns per CTA
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kPrefetch = 3;     // key tiles prefetched into L2 beyond the stages in flight
-constexpr int kMaxCh = 5;        // CTA 0: 4 latent chunks + 1 rope chunk per key tile
+constexpr int kRopeHalf = 32;    // rope dimensions per CTA (64-byte rows, 64-byte swizzle)
 constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
-constexpr int kQRopeBytes = BM * CH * 2;
+constexpr int kRopeChunk = BN * kRopeHalf * 2;            // 4 KiB of k_rope per key tile
+constexpr int kStageBytes = 4 * kKVChunk + kRopeChunk;    // 4 latent chunks + the rope half
+constexpr int kQRopeBytes = BM * kRopeHalf * 2;
 constexpr int kPBytes = BM * BN * 2;    // the P tile: 128 rows x 64 keys bf16, 128B-swizzled
 constexpr int kPQuadBytes = 16 * BN * 2;   // one quadrant's own P rows (contiguous, 2 KiB)
 // Score exchange: the peer's 64 rows as fp16 in the receiving softmax
@@ -91,7 +93,7 @@ constexpr int kColQ = 256;
 constexpr int kColS = 384;       // + 64 * buffer
 
 constexpr int OFF_KV = 0;
-constexpr int OFF_QR = OFF_KV + kStages * kMaxCh * kKVChunk;
+constexpr int OFF_QR = OFF_KV + kStages * kStageBytes;
 constexpr int OFF_P = OFF_QR + kQRopeBytes;
 constexpr int OFF_RX = OFF_P + kPBytes;                        // two receive buffers
 constexpr int OFF_AF = OFF_RX + 2 * kRxStride;                 // [kAfBufs][BM] floats
@@ -102,7 +104,8 @@ constexpr int kNumBars = 48;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
 constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(OFF_QR % 1024 == 0 && OFF_P % 1024 == 0, "128B-swizzled tiles need 1 KiB alignment");
+static_assert(kStageBytes % 1024 == 0 && OFF_QR % 1024 == 0 && OFF_P % 1024 == 0,
+              "swizzled tiles need 1 KiB alignment");
 static_assert(OFF_RX % 16 == 0 && kRxStride % 16 == 0 && OFF_AF % 16 == 0, "async store alignment");
 static_assert(kThreads == 32 * (kWarpPV + 1), "warp roles");
 
@@ -369,18 +372,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       auto prefetch = [&](int b, int k) {
         const int row = key_row(b, k);
         for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_ckv, (int)rank * kHalf + c * CH, row);
-        if (rank == 0) tma_prefetch_2d(&tm_krope, 0, row);
+        tma_prefetch_2d(&tm_krope, kRopeHalf * (int)rank, row);
       };
       Piece pc;
       bool have = piece_first(a, cl, beg, end, W, pc);
       int g = 0, pi = 0, issued = 0, qr_issued = 0;
       bool alive = true;
       while (alive && have) {
-        if (rank == 0) {   // q_rope rows of this piece, once Q.K^T of the previous piece is done
+        {   // this CTA's q_rope half of the piece's rows, once Q.K^T of the previous piece is done
           if (pi >= 1 && !wait(BAR(B_QR_EMPTY), (pi - 1) & 1, st, limit, W_Q_EMPTY)) break;
           ++qr_issued;
           mbar_expect_tx(BAR(B_QR_FULL), kQRopeBytes);
-          tma_load_2d(sbase + OFF_QR, &tm_qrope, BAR(B_QR_FULL), 0,
+          tma_load_2d(sbase + OFF_QR, &tm_qrope, BAR(B_QR_FULL), kRopeHalf * (int)rank,
                       (int)((long long)pc.b * nrows + pc.rt * BM));
         }
         for (int j = pc.t0 + kStages; j < pc.t0 + kStages + kPrefetch && j < pc.t1; ++j)
@@ -393,12 +396,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
             break;
           }
           const int row = key_row(pc.b, j * BN);
-          mbar_expect_tx(BAR(B_KV_FULL + stg), (rank == 0 ? 5 : 4) * kKVChunk);
-          const uint32_t dst = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+          mbar_expect_tx(BAR(B_KV_FULL + stg), kStageBytes);
+          const uint32_t dst = sbase + OFF_KV + stg * kStageBytes;
           for (int c = 0; c < 4; ++c)
             tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
                         (int)rank * kHalf + c * CH, row);
-          if (rank == 0) tma_load_2d(dst + 4 * kKVChunk, &tm_krope, BAR(B_KV_FULL + stg), 0, row);
+          tma_load_2d(dst + 4 * kKVChunk, &tm_krope, BAR(B_KV_FULL + stg), kRopeHalf * (int)rank, row);
           issued = g + 1;
           if (j + kStages + kPrefetch < pc.t1) prefetch(pc.b, (j + kStages + kPrefetch) * BN);
         }
@@ -421,7 +424,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       bool alive = true;
       while (alive && have) {
         alive = wait(BAR(B_Q_READY), pi & 1, st, limit, W_Q);
-        if (alive && rank == 0) alive = wait(BAR(B_QR_FULL), pi & 1, st, limit, W_Q);
+        if (alive) alive = wait(BAR(B_QR_FULL), pi & 1, st, limit, W_Q);
         for (int j = pc.t0; alive && j < pc.t1; ++j, ++g) {
           const int stg = g % kStages, buf = g & 1;
           alive = wait(BAR(B_KV_FULL + stg), (g / kStages) & 1, st, limit, W_KV_FULL);
@@ -431,25 +434,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           if (!alive) break;
           tc_fence_after();
           const uint32_t d = tmem + kColS + 64 * buf;
-          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+          const uint32_t kv = sbase + OFF_KV + stg * kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < kHalf / 16; ++kk) {     // latent half: A = q_lat in TMEM
             uint64_t bd = smem_desc(kv + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
             mma_bf16_ts(d, tmem + kColQ + 8 * kk, bd, kIdescQK, kk > 0);
           }
-          if (rank == 0) {
 #pragma unroll
-            for (int kk = 0; kk < CH / 16; ++kk) {      // rope: A = q_rope in smem
-              uint64_t ad = smem_desc(sbase + OFF_QR + kk * 32, 16, 1024);
-              uint64_t bd = smem_desc(kv + 4 * kKVChunk + kk * 32, 16, 1024);
-              mma_bf16(d, ad, bd, kIdescQK, 1);
-            }
+          for (int kk = 0; kk < kRopeHalf / 16; ++kk) {   // rope half: A = q_rope half in smem
+            uint64_t ad = smem_desc_sw64(sbase + OFF_QR + kk * 32, 16, 512);
+            uint64_t bd = smem_desc_sw64(kv + 4 * kKVChunk + kk * 32, 16, 512);
+            mma_bf16(d, ad, bd, kIdescQK, 1);
           }
           mma_commit(BAR(B_S_FULL + buf));
         }
         if (!alive) break;
         mma_commit(BAR(B_Q_EMPTY));                 // Q (and q_rope) may be reloaded
-        if (rank == 0) mma_commit(BAR(B_QR_EMPTY));
+        mma_commit(BAR(B_QR_EMPTY));
         ++pi;
         have = piece_next(a, end, W, pc);
       }
@@ -479,7 +480,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           // arm the peer's P rows of tile g+1 before our commit lets the peer send them
           if (g + 1 < G) { mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes); ++p_armed; }
           tc_fence_after();
-          const uint32_t kv = sbase + OFF_KV + stg * kMaxCh * kKVChunk;
+          const uint32_t kv = sbase + OFF_KV + stg * kStageBytes;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             // A = P (K-major, 128B rows); B = V = c_kv columns of this CTA,
@@ -1039,10 +1040,11 @@ EncodeTiledFn encoder() {
 
 }  // namespace
 
-// 2-D bf16 tensor map with a 128-byte swizzle: rows x cols (row stride
-// cols * 2 bytes), box = box_rows x box_cols.
+// 2-D bf16 tensor map: rows x cols (row stride row_stride_elems, or cols,
+// elements), box = box_rows x box_cols, 128- or 64-byte swizzle.
 CUresult encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                   uint32_t box_cols, uint32_t box_rows, uint64_t row_stride_elems) {
+                   uint32_t box_cols, uint32_t box_rows, uint64_t row_stride_elems,
+                   int swizzle_bytes) {
   EncodeTiledFn fn = encoder();
   if (!fn) return CUDA_ERROR_NOT_FOUND;
   cuuint64_t dims[2] = {cols, rows};
@@ -1050,7 +1052,8 @@ CUresult encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
@@ -1079,9 +1082,9 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
   const long long kv_rows = a.page_size ? (long long)a.num_pages * a.page_size
                                         : (long long)a.B * a.t_stride;
   CUtensorMap tqr, tck, tkr;
-  if (encode_2d(&tqr, a.q_rope, rows, 64, CH, BM) != CUDA_SUCCESS ||
+  if (encode_2d(&tqr, a.q_rope, rows, 64, kRopeHalf, BM, 0, 64) != CUDA_SUCCESS ||
       encode_2d(&tck, a.c_kv, kv_rows, 512, CH, BN) != CUDA_SUCCESS ||
-      encode_2d(&tkr, a.k_rope, kv_rows, 64, CH, BN) != CUDA_SUCCESS)
+      encode_2d(&tkr, a.k_rope, kv_rows, 64, kRopeHalf, BN, 0, 64) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
 
   const bool simt_proj = a.flags & KDTV_FLAG_SIMT_PROJ;
