@@ -123,8 +123,8 @@ enum Bar : int {
   B_P_FULL = B_AF_FULL + kAfBufs,    // our softmax wrote its P rows
   B_P_RX = B_P_FULL + 1,             // the peer's P rows landed (tx)
   B_P_EMPTY = B_P_RX + 1,            // [2] P.V of an even / odd tile completed in both CTAs
-  B_O_FULL = B_P_EMPTY + 2,
-  B_MMA_DONE = B_O_FULL + 1,         // both MMA issuers drained
+  B_O_FULL = B_P_EMPTY + 2,          // [2] a piece's O is complete, for the even / odd-tile warps
+  B_MMA_DONE = B_O_FULL + 2,         // both MMA issuers drained
   B_STALL = B_MMA_DONE + 1,
   B_MREF = B_STALL + 1,              // [2 parities][4 quadrants] reference maxima published
   B_LSUM = B_MREF + 8,               // the odd-tile softmax warps published their (m, l)
@@ -319,7 +319,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     // phase of the barrier it waits on in order.
     mbar_init(BAR(B_P_EMPTY + 0), 2);
     mbar_init(BAR(B_P_EMPTY + 1), 2);
-    mbar_init(BAR(B_O_FULL), 1);
+    mbar_init(BAR(B_O_FULL + 0), 1);
+    mbar_init(BAR(B_O_FULL + 1), 1);
     mbar_init(BAR(B_MMA_DONE), 2);
     mbar_init(BAR(B_STALL), 1);
     for (int i = 0; i < 8; ++i) mbar_init(BAR(B_MREF + i), 1);
@@ -493,9 +494,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           mma_commit_multicast(BAR(B_P_EMPTY + (g & 1)), 0x3);   // both CTAs may overwrite P
         }
         if (!alive) break;
-        mma_commit(BAR(B_O_FULL));                 // the piece's O is complete
-        ++pi;
+        // the piece's O is complete: tell the warps that write it out (those that
+        // took the piece's last tile when another piece follows, else all)
         have = piece_next(a, end, W, pc);
+        if (!have || ((g - 1) & 1) == 0) mma_commit(BAR(B_O_FULL + 0));
+        if (!have || ((g - 1) & 1) == 1) mma_commit(BAR(B_O_FULL + 1));
+        ++pi;
       }
       // After an abort: let the peer's P rows of an armed, unconsumed phase land.
       if (!alive && p_armed > 0) drain_wait(BAR(B_P_RX), (p_armed - 1) & 1, 200000ull);
@@ -627,15 +631,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       int next_af = par;
       // Writes O columns [col0, col0 + 32 nch32) of rows 32q .. 32q+31 of a piece
       // (row tile rt, partial slot `slot`) once its P.V completed, then frees O.
-      auto write_o = [&](int slot, int rt, int phase, int col0, int nch32) -> bool {
-        if (!__all_sync(0xffffffffu, wait(BAR(B_O_FULL), phase, st, limit, W_O_FULL))) return false;
+      int o_waits = 0;                            // phases of B_O_FULL + par consumed so far
+      auto write_o = [&](int slot, int rt, bool free_o, int col0, int nch32) -> bool {
+        if (!__all_sync(0xffffffffu, wait(BAR(B_O_FULL + par), o_waits & 1, st, limit, W_O_FULL)))
+          return false;
+        ++o_waits;
         tc_fence_after();
         store_o_quadrant(tmem + (static_cast<uint32_t>(32 * q) << 16) + kColO + col0,
                          a.part_o + ((long long)slot * BM + 32 * q) * a.d_c + rank * kHalf + col0, a.d_c,
                          nrows - (rt * BM + 32 * q), nch32);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(B_O_FREE));   // the next piece may overwrite O
+        if (free_o && lane == 0) mbar_arrive(BAR(B_O_FREE));   // the next piece may overwrite O
         return true;
       };
       while (alive && have) {
@@ -896,12 +903,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         }
         // O write-out.  After the pair's last piece the 8 softmax warps write 128
         // columns each.  When another piece follows, the 4 warps that took this
-        // piece's last tile write all 256 columns while the other 4 go on with
-        // the next piece's first tile (B_O_FREE counts 4 arrivals).
+        // piece's last tile write all 256 columns and free O (B_O_FREE counts 4
+        // arrivals) while the other 4 go on with the next piece's first tile.
+        // B_O_FULL + par completes only for pieces that this parity writes, so
+        // each warp sees its phases in order.
         Piece nx = pc;
         have = piece_next(a, end, W, nx);
-        if (!have ? !write_o(pc.slot, pc.rt, pi & 1, 128 * par, 4)
-                  : (((g - 1) & 1) == par && !write_o(pc.slot, pc.rt, pi & 1, 0, 8))) {
+        if (!have ? !write_o(pc.slot, pc.rt, false, 128 * par, 4)
+                  : (((g - 1) & 1) == par && !write_o(pc.slot, pc.rt, true, 0, 8))) {
           alive = false;
           break;
         }

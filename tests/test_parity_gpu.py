@@ -170,6 +170,26 @@ def test_bf16_forced_splits(path, chunk):
     check(wl, got, all_nodes(wl))
 
 
+@pytest.mark.parametrize("chunk", [0, 64 * 3, 64 * 7, 64 * 11])
+def test_tc_piece_boundaries_match_simt(chunk):
+    """Work units per CTA pair forced to 3, 7 or 11 key tiles (or the plan's own
+    choice) on rows of 16 nodes x 64 heads = 8 row tiles per request: pairs
+    cross row-tile boundaries, some pieces are a single key tile, and one pair
+    may hold three pieces.  The whole tensor-core output matches the SIMT path,
+    and sampled nodes match the oracle."""
+    wl = small("s_pieces", B=3, N=16, prefix=("uniform", 200, 1300))
+    _skip_tc(TC, wl)
+    a, st1, _ = run(wl, flags=TC, kv_chunk=chunk)
+    b, st2, _ = run(wl, flags=SIMT)
+    assert st1 == st2 == 0
+    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert rel <= BF16_REL
+    rows_bad = (np.abs(a - b).reshape(-1, a.shape[-1]).max(axis=1) >
+                0.05 * (np.abs(b).reshape(-1, b.shape[-1]).max(axis=1) + 1e-3))
+    assert int(rows_bad.sum()) == 0
+    check(wl, a, [(bi, i) for bi in range(wl.spec.B) for i in (0, wl.spec.N // 2, wl.spec.N - 1)])
+
+
 @pytest.mark.parametrize("path", list(PATH_IDS))
 @pytest.mark.parametrize("case", ["single_node", "empty_prefix", "star", "max_nodes_chain",
                                   "few_heads"])
