@@ -36,11 +36,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # DRAM bytes (read + write) of one attention-kernel launch, from an ncu
-# capture of that workload (profiles/attn_tc_kernel_<workload>.md), keyed by
-# the SHA-256 of the kernel source the capture was taken on: a changed kernel
-# reports null until it is captured again.
+# capture of that workload, keyed by the SHA-256 of the kernel source the
+# capture was taken on: a changed kernel reports null until it is captured
+# again.
 ATTN_TRAFFIC = {
-    "kimi_single": ("58352b7385c8aed51bca8c6b7cf443084794828645df2ae9089c12415d2ba310", 9626880),
+    "kimi_single": ("9b3eea0d0592fc26da7c4f300da2204c0714999d0b3e8814dead95de923d8f22", 9594880),
+    "long": ("9b3eea0d0592fc26da7c4f300da2204c0714999d0b3e8814dead95de923d8f22", 1047564288),
 }
 
 

@@ -24,7 +24,7 @@ order a reader would check them:
   5. latent mix    o_lat = sum_t p_t c_kv[t]
   6. up-project    out[b,i,h,:] = W_UV[h] o_lat
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * a node sees itself (forced by the chain == causal invariant);
   * W_UK is [H, d_nope, d_c] with k_nope = W_UK[h] c; W_UV is [H, d_v, d_c];
   * k_rope is one shared head [T, d_rope]; q_rope / k_rope arrive rotated;
