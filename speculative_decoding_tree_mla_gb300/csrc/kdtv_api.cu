@@ -85,7 +85,7 @@ int make_plan(const kdtv_dims* d, Plan* p) {
     p->chunk = 64;
     p->splits = 1;
     p->off_qlat = off;    off = align256(off + rows * d->d_c * sizeof(float));
-    p->off_part_o = off;  off = align256(off + (size_t)p->slots * 128 * d->d_c * sizeof(float));
+    p->off_part_o = off;  off = align256(off + (size_t)p->slots * 128 * d->d_c * sizeof(__nv_bfloat16));
     p->off_part_ml = off; off = align256(off + (size_t)p->slots * 128 * 2 * sizeof(float));
     p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
     p->off_sk = off;      off = align256(off + (size_t)(kSkHeader + 3 * R + clusters) * sizeof(int));
@@ -166,6 +166,8 @@ extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const vo
   a.part_ml = reinterpret_cast<float*>(ws + p.off_part_ml);
   a.o_lat = reinterpret_cast<float*>(ws + p.off_olat);
   if (p.tensor_core) {
+    a.part_o = nullptr;
+    a.part_o16 = reinterpret_cast<__nv_bfloat16*>(ws + p.off_part_o);
     a.sk = reinterpret_cast<int*>(ws + p.off_sk);
     a.anc_g = reinterpret_cast<uint32_t*>(ws + p.off_anc);
     a.rt_count = p.rt_count;

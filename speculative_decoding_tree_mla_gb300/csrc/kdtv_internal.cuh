@@ -67,7 +67,8 @@ struct Args {
   float* out;
   DeviceStatus* status;
   void* q_lat;            // fp32 (SIMT) or bf16 (tensor core) [rows, d_c]
-  float* part_o;          // [splits, rows, d_c], or [slots, 128, d_c] with a stream-K plan
+  float* part_o;          // [splits, rows, d_c] fp32 (split layout)
+  __nv_bfloat16* part_o16;  // [slots, 128, d_c] bf16 with a stream-K plan (unnormalised o_lat)
   float* part_ml;         // [splits, rows, 2] or [slots, 128, 2]  (running max m, sum l)
   float* o_lat;           // [rows, d_c]
   // Stream-K plan of the tensor-core attention (nullptr: split layout).

@@ -235,7 +235,10 @@ __global__ void __launch_bounds__(128) combine_kernel(Args a) {
   for (int d = threadIdx.x; d < a.d_c; d += blockDim.x) {
     float acc = 0.f;
     for (int s = 0; s < S; ++s)
-      if (w_s[s] != 0.f) acc = fmaf(w_s[s], a.part_o[(pr.base + s * pr.step) * a.d_c + d], acc);
+      if (w_s[s] != 0.f) {
+        const long long i = (pr.base + s * pr.step) * a.d_c + d;
+        acc = fmaf(w_s[s], a.sk ? __bfloat162float(a.part_o16[i]) : a.part_o[i], acc);
+      }
     a.o_lat[row * a.d_c + d] = acc * inv_l;
   }
 }

@@ -234,21 +234,22 @@ __device__ __forceinline__ void rescale_o_rows(uint32_t taddr, float alpha_a, fl
 }
 
 // Stores 32 * nch32 O columns of the 32 rows of a warp's TMEM lane quadrant
-// (ta0: TMEM address of the quadrant's first lane and column; dst0: row 0,
-// column 0 of the destination, rows d_c floats apart; rows >= nvalid are
-// skipped).  Reads the .16x256b layout (rows t/4 and t/4 + 8 of each 16-row
-// half, column pairs 8k + 2c); a pair exchange between threads c and c ^ 1
-// gives each thread 4 consecutive columns, so one warp store covers 64
+// as bf16 (ta0: TMEM address of the quadrant's first lane and column; dst0:
+// row 0, column 0 of the destination, rows d_c elements apart; rows >= nvalid
+// are skipped).  Reads the .16x256b layout (rows t/4 and t/4 + 8 of each
+// 16-row half, column pairs 8k + 2c); a pair exchange between threads c and
+// c ^ 1 gives each thread 4 consecutive columns, so one warp store covers 32
 // contiguous bytes of each of 8 rows.  Out of line: it runs once per piece.
-__device__ __noinline__ void store_o_quadrant(uint32_t ta0, float* dst0, int d_c, int nvalid, int nch32) {
+__device__ __noinline__ void store_o_quadrant(uint32_t ta0, __nv_bfloat16* dst0, int d_c, int nvalid,
+                                              int nch32) {
   const int lane = threadIdx.x & 31, c = lane & 3;
   const bool odd = c & 1;
 #pragma unroll 1
   for (int hh = 0; hh < 2; ++hh) {
     const int r = 16 * hh + (lane >> 2);                 // rows r, r + 8
     const bool wa = r < nvalid, wb = r + 8 < nvalid;
-    float* pra = dst0 + (long long)r * d_c + (odd ? 2 * c + 6 : 2 * c);
-    float* prb = pra + 8 * d_c;
+    __nv_bfloat16* pra = dst0 + (long long)r * d_c + (odd ? 2 * c + 6 : 2 * c);
+    __nv_bfloat16* prb = pra + 8 * d_c;
     const uint32_t ta = ta0 + (static_cast<uint32_t>(16 * hh) << 16);
 #pragma unroll 1
     for (int cc = 0; cc < nch32; ++cc) {                 // 32 columns per load
@@ -264,16 +265,16 @@ __device__ __noinline__ void store_o_quadrant(uint32_t ta0, float* dst0, int d_c
         const uint32_t ra1 = __shfl_xor_sync(0xffffffffu, sa1, 1);
         const uint32_t rb0 = __shfl_xor_sync(0xffffffffu, sb0, 1);
         const uint32_t rb1 = __shfl_xor_sync(0xffffffffu, sb1, 1);
-        const float4 oa = odd ? make_float4(__uint_as_float(ra0), __uint_as_float(ra1),
-                                            __uint_as_float(v[4 * k + 4]), __uint_as_float(v[4 * k + 5]))
-                              : make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]),
-                                            __uint_as_float(ra0), __uint_as_float(ra1));
-        const float4 ob = odd ? make_float4(__uint_as_float(rb0), __uint_as_float(rb1),
-                                            __uint_as_float(v[4 * k + 6]), __uint_as_float(v[4 * k + 7]))
-                              : make_float4(__uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]),
-                                            __uint_as_float(rb0), __uint_as_float(rb1));
-        if (wa) *reinterpret_cast<float4*>(pra + 32 * cc + 8 * k) = oa;
-        if (wb) *reinterpret_cast<float4*>(prb + 32 * cc + 8 * k) = ob;
+        const uint2 oa = odd ? make_uint2(pack_bf16x2(__uint_as_float(ra0), __uint_as_float(ra1)),
+                                          pack_bf16x2(__uint_as_float(v[4 * k + 4]), __uint_as_float(v[4 * k + 5])))
+                             : make_uint2(pack_bf16x2(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1])),
+                                          pack_bf16x2(__uint_as_float(ra0), __uint_as_float(ra1)));
+        const uint2 ob = odd ? make_uint2(pack_bf16x2(__uint_as_float(rb0), __uint_as_float(rb1)),
+                                          pack_bf16x2(__uint_as_float(v[4 * k + 6]), __uint_as_float(v[4 * k + 7])))
+                             : make_uint2(pack_bf16x2(__uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3])),
+                                          pack_bf16x2(__uint_as_float(rb0), __uint_as_float(rb1)));
+        if (wa) *reinterpret_cast<uint2*>(pra + 32 * cc + 8 * k) = oa;
+        if (wb) *reinterpret_cast<uint2*>(prb + 32 * cc + 8 * k) = ob;
       }
     }
   }
@@ -638,7 +639,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         ++o_waits;
         tc_fence_after();
         store_o_quadrant(tmem + (static_cast<uint32_t>(32 * q) << 16) + kColO + col0,
-                         a.part_o + ((long long)slot * BM + 32 * q) * a.d_c + rank * kHalf + col0, a.d_c,
+                         a.part_o16 + ((long long)slot * BM + 32 * q) * a.d_c + rank * kHalf + col0, a.d_c,
                          nrows - (rt * BM + 32 * q), nch32);
         tc_fence_before();
         __syncwarp();

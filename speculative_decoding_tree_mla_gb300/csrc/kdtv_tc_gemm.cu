@@ -235,48 +235,42 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   const int S = *s_max;
 
   // o_lat rows -> bf16, 128-byte swizzled K-major operand: row r, 8-column unit u.
-  // Each pass merges UP_BATCH units per thread with all their loads in flight.
+  // Each pass merges UP_BATCH units per thread; the bf16 partials of up to four
+  // pieces are loaded per step, 4 x UP_BATCH x 16 bytes in flight per thread.
   for (int base = tid; base < UP_NR * 64; base += UP_THREADS * UP_BATCH) {
     float acc[UP_BATCH][8];
 #pragma unroll
     for (int uu = 0; uu < UP_BATCH; ++uu)
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[uu][e] = 0.f;
-    // Two splits per step: 2 x UP_BATCH x 32 bytes of loads in flight per thread.
-    for (int s0 = 0; s0 < S; s0 += 2) {
-      float4 x[2][UP_BATCH][2];
-      float ws[2][UP_BATCH];
+    for (int s0 = 0; s0 < S; s0 += 4) {
+      uint4 x[4][UP_BATCH];
+      float ws[4][UP_BATCH];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
+      for (int q = 0; q < 4; ++q) {
         const int s = s0 + q;
 #pragma unroll
         for (int uu = 0; uu < UP_BATCH; ++uu) {
           const int idx = base + uu * UP_THREADS;
           const int r = idx >> 6, u = idx & 63;
           ws[q][uu] = (s < S && idx < UP_NR * 64 && r < nr) ? wts[r * UP_MAX_SPLITS + s] : 0.f;
-          if (ws[q][uu] != 0.f) {
-            const float4* src = reinterpret_cast<const float4*>(
-                a.part_o + (pr_base[r] + (long long)s * pr_step[r]) * 512 + 8 * u);
-            x[q][uu][0] = src[0];
-            x[q][uu][1] = src[1];
-          } else {
-            x[q][uu][0] = x[q][uu][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
+          x[q][uu] = ws[q][uu] != 0.f
+                         ? *reinterpret_cast<const uint4*>(
+                               a.part_o16 + (pr_base[r] + (long long)s * pr_step[r]) * 512 + 8 * u)
+                         : make_uint4(0u, 0u, 0u, 0u);
         }
       }
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int uu = 0; uu < UP_BATCH; ++uu) {
           const float w = ws[q][uu];
-          acc[uu][0] = fmaf(w, x[q][uu][0].x, acc[uu][0]);
-          acc[uu][1] = fmaf(w, x[q][uu][0].y, acc[uu][1]);
-          acc[uu][2] = fmaf(w, x[q][uu][0].z, acc[uu][2]);
-          acc[uu][3] = fmaf(w, x[q][uu][0].w, acc[uu][3]);
-          acc[uu][4] = fmaf(w, x[q][uu][1].x, acc[uu][4]);
-          acc[uu][5] = fmaf(w, x[q][uu][1].y, acc[uu][5]);
-          acc[uu][6] = fmaf(w, x[q][uu][1].z, acc[uu][6]);
-          acc[uu][7] = fmaf(w, x[q][uu][1].w, acc[uu][7]);
+          const uint32_t wv[4] = {x[q][uu].x, x[q][uu].y, x[q][uu].z, x[q][uu].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[uu][2 * j] = fmaf(w, __uint_as_float(wv[j] << 16), acc[uu][2 * j]);
+            acc[uu][2 * j + 1] = fmaf(w, __uint_as_float(wv[j] & 0xffff0000u), acc[uu][2 * j + 1]);
+          }
         }
     }
 #pragma unroll
@@ -340,8 +334,8 @@ bool absorb_tc_ok(const Args& a) {
 }
 
 bool combine_uproj_tc_ok(const Args& a) {
-  return a.dtype == KDTV_BF16 && a.d_c == 512 && a.d_v == 128 &&
-         (a.sk != nullptr || a.splits <= UP_MAX_SPLITS);
+  // reads the bf16 partials of a stream-K plan
+  return a.dtype == KDTV_BF16 && a.d_c == 512 && a.d_v == 128 && a.sk != nullptr;
 }
 
 cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st, bool after_plan) {
