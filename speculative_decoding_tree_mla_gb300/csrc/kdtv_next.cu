@@ -121,19 +121,36 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
 }
 
 // ---- best-first tree build ----------------------------------------------------------------
-// One CTA per request.  The frontier holds every candidate child (parent
-// node, rank k) with its float32 score; each step takes the best candidate
-// (highest score, then lower parent index, then lower k) with a block-wide
-// reduction, appends it as the next node and adds its K children.
-constexpr int kBuildThreads = 128;
+// One warp per request.  Candidate child k of node u (slot u K + k) is one
+// 64-bit word whose unsigned order is the preference order: the score's
+// order-preserving bits in the high half (higher score first), ~key in the
+// low half (key = u 65536 + k, so a lower parent and then a lower k win
+// ties); 0 is a taken or absent child.  Each node also keeps the word of its
+// best remaining child, so a step is:
+//   * a warp-wide maximum over the n node words (two 32-bit reductions: the
+//     high half, then the low half among the lanes holding the highest);
+//   * the winner becomes node n;
+//   * the lanes recompute the best remaining child of the winner's parent and
+//     the best child of the new node (K children each, one per lane).
+// The proposals of the depths a tree can reach (min(D, N - 1)) are staged in
+// shared memory first; the nodes are written out at the end.
+constexpr int kBuildThreads = 32;
 
-struct Cand {
-  float s;
-  int key;   // parent * 65536 + k  (lower is preferred on equal scores)
-};
-
-__device__ __forceinline__ bool better(const Cand& a, const Cand& b) {
-  return a.s > b.s || (a.s == b.s && a.key < b.key);
+__device__ __forceinline__ uint32_t order_bits(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float from_order_bits(uint32_t o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+__device__ __forceinline__ unsigned long long cand_word(float s, int key) {
+  return ((unsigned long long)order_bits(s) << 32) | (uint32_t)~(uint32_t)key;
+}
+// Maximum of a 64-bit word over the warp.
+__device__ __forceinline__ unsigned long long warp_max_word(unsigned long long w) {
+  const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(w >> 32));
+  const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(w >> 32) == hi ? (uint32_t)w : 0u);
+  return ((unsigned long long)hi << 32) | lo;
 }
 
 __global__ void __launch_bounds__(kBuildThreads) tree_build_kernel(
@@ -142,75 +159,86 @@ __global__ void __launch_bounds__(kBuildThreads) tree_build_kernel(
     int32_t* __restrict__ token_out, int32_t* __restrict__ depth_out,
     float* __restrict__ score_out, int32_t* __restrict__ n_out) {
   extern __shared__ __align__(16) unsigned char sbuf[];
-  float* cs = reinterpret_cast<float*>(sbuf);               // [N*K] candidate scores
-  int* ck = reinterpret_cast<int*>(cs + N * K);             // [N*K] keys (-1 = taken/empty)
-  int* ndepth = ck + N * K;                                 // [N]
-  float* nscore = reinterpret_cast<float*>(ndepth + N);     // [N]
-  __shared__ Cand red[kBuildThreads / 32];
-  __shared__ Cand best_s;
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int Ds = D < N - 1 ? D : N - 1;                      // depths whose proposals are used
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(sbuf);   // [N*K]
+  unsigned long long* nbest = cand + N * K;                 // [N] best remaining child per node
+  int* ndepth = reinterpret_cast<int*>(nbest + N);          // [N]
+  float* lps = reinterpret_cast<float*>(ndepth + N);        // [Ds*K] staged log-probabilities
+  int* tks = reinterpret_cast<int*>(lps + Ds * K);          // [Ds*K] staged tokens
+  int* opar = tks + Ds * K;                                 // [N] outputs, written out at the end
+  int* otok = opar + N;
+  float* osco = reinterpret_cast<float*>(otok + N);
+  const int b = blockIdx.x, lane = threadIdx.x;
   const float* lp = logp + (long long)b * D * K;
   const int32_t* tk = tokens + (long long)b * D * K;
+
+#pragma unroll 4
+  for (int i = lane; i < Ds * K; i += 32) { lps[i] = lp[i]; tks[i] = tk[i]; }
+  __syncwarp();
+  // the root and its children
+  {
+    unsigned long long m = 0ull;
+    if (Ds > 0)
+      for (int k = lane; k < K; k += 32) {
+        const unsigned long long w = cand_word(__fadd_rn(0.f, lps[k]), k);
+        cand[k] = w;
+        m = max(m, w);
+      }
+    m = warp_max_word(m);
+    if (lane == 0) {
+      nbest[0] = m;
+      opar[0] = -1; otok[0] = root_token[b]; osco[0] = 0.f;
+      ndepth[0] = 0;
+    }
+  }
+  __syncwarp();
+  int n = 1;
+  while (n < N) {
+    unsigned long long m = 0ull;
+    for (int i = lane; i < n; i += 32) m = max(m, nbest[i]);
+    const unsigned long long win = warp_max_word(m);
+    if (win == 0ull) break;                       // frontier empty
+    const float sw = from_order_bits((uint32_t)(win >> 32));
+    const int key = (int)~(uint32_t)win;
+    const int u = key >> 16, k = key & 0xffff;
+    const int d = ndepth[u];
+    const bool grow = d + 1 < Ds;
+    // the parent's remaining children, and the new node's children
+    unsigned long long mu = 0ull, mn = 0ull;
+    for (int kk = lane; kk < K; kk += 32) {
+      unsigned long long wu = cand[u * K + kk];
+      if (kk == k) { wu = 0ull; cand[u * K + kk] = 0ull; }   // taken
+      mu = max(mu, wu);
+      if (grow) {
+        const unsigned long long wn = cand_word(__fadd_rn(sw, lps[(d + 1) * K + kk]), n * 65536 + kk);
+        cand[n * K + kk] = wn;
+        mn = max(mn, wn);
+      }
+    }
+    mu = warp_max_word(mu);
+    mn = warp_max_word(mn);
+    if (lane == 0) {
+      nbest[u] = mu;
+      nbest[n] = mn;
+      opar[n] = u; otok[n] = tks[d * K + k]; osco[n] = sw;
+      ndepth[n] = d + 1;
+    }
+    __syncwarp();
+    ++n;
+  }
+  __syncwarp();
   int32_t* par = parent_out + (long long)b * N;
   int32_t* tok = token_out + (long long)b * N;
   int32_t* dep = depth_out + (long long)b * N;
   float* sco = score_out + (long long)b * N;
-
-  for (int i = tid; i < N * K; i += blockDim.x) ck[i] = -1;
-  if (tid == 0) {
-    par[0] = -1; tok[0] = root_token[b]; dep[0] = 0; sco[0] = 0.f;
-    ndepth[0] = 0; nscore[0] = 0.f;
+  for (int i = lane; i < N; i += 32) {
+    const bool live = i < n;
+    par[i] = live ? opar[i] : -1;
+    tok[i] = live ? otok[i] : -1;
+    dep[i] = live ? ndepth[i] : -1;
+    sco[i] = live ? osco[i] : -INFINITY;
   }
-  __syncthreads();
-  if (D > 0)
-    for (int k = tid; k < K; k += blockDim.x) { cs[k] = 0.f + lp[k]; ck[k] = k; }
-  __syncthreads();
-  int n = 1;
-  while (n < N) {
-    Cand mine{-INFINITY, 0x7fffffff};
-    bool any = false;
-    for (int i = tid; i < n * K; i += blockDim.x) {
-      if (ck[i] < 0) continue;
-      Cand c{cs[i], ck[i]};
-      if (!any || better(c, mine)) { mine = c; any = true; }
-    }
-    for (int off = 16; off; off >>= 1) {
-      Cand o{__shfl_xor_sync(0xffffffffu, mine.s, off), __shfl_xor_sync(0xffffffffu, mine.key, off)};
-      const bool oany = __shfl_xor_sync(0xffffffffu, (int)any, off);
-      if (oany && (!any || better(o, mine))) { mine = o; any = true; }
-    }
-    if ((tid & 31) == 0) red[tid >> 5] = any ? mine : Cand{-INFINITY, -1};
-    __syncthreads();
-    if (tid == 0) {
-      Cand bb{-INFINITY, -1};
-      for (int w = 0; w < kBuildThreads / 32; ++w) {
-        const Cand c = red[w];
-        if (c.key < 0) continue;
-        if (bb.key < 0 || better(c, bb)) bb = c;
-      }
-      best_s = bb;
-    }
-    __syncthreads();
-    const Cand bb = best_s;
-    if (bb.key < 0) break;                       // frontier empty
-    const int u = bb.key >> 16, k = bb.key & 0xffff;
-    const int d = ndepth[u];
-    if (tid == 0) {
-      ck[u * K + k] = -1;                        // taken
-      par[n] = u; tok[n] = tk[d * K + k]; dep[n] = d + 1; sco[n] = bb.s;
-      ndepth[n] = d + 1; nscore[n] = bb.s;
-    }
-    __syncthreads();
-    if (d + 1 < D)
-      for (int kk = tid; kk < K; kk += blockDim.x) {
-        cs[n * K + kk] = __fadd_rn(bb.s, lp[(d + 1) * K + kk]);
-        ck[n * K + kk] = n * 65536 + kk;
-      }
-    ++n;
-    __syncthreads();
-  }
-  for (int i = n + tid; i < N; i += blockDim.x) { par[i] = -1; tok[i] = -1; dep[i] = -1; sco[i] = -INFINITY; }
-  if (tid == 0) n_out[b] = n;
+  if (lane == 0) n_out[b] = n;
 }
 
 }  // namespace
@@ -268,7 +296,9 @@ extern "C" int kdtv_tree_build(int B, int D, int K, int N, const float* logp,
   if ((D > 0 && (!logp || !tokens)) || !root_token || !parent || !token || !depth || !score ||
       !n_nodes)
     return KDTV_ERR_INVALID_ARG;
-  const size_t sm = (size_t)N * K * (sizeof(float) + sizeof(int)) + (size_t)N * 8;
+  const int Ds = D < N - 1 ? D : N - 1;
+  const size_t sm = (size_t)(N * K + N) * sizeof(unsigned long long) + (size_t)N * 4 * sizeof(int) +
+                    (size_t)Ds * K * (sizeof(float) + sizeof(int));
   if (sm > 48 * 1024 &&
       cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sm) != cudaSuccess)
