@@ -42,13 +42,17 @@
 extern "C" {
 #endif
 
-#define KDTV_ABI_VERSION 1
+#define KDTV_ABI_VERSION 2
 
 /* Element type of q_nope, q_rope, W_UK, W_UV, c_kv and k_rope.  `out` is
  * always float32. */
 enum kdtv_dtype {
-  KDTV_F32 = 0,   /* every input float32; computed on CUDA cores in fp32   */
-  KDTV_BF16 = 1   /* every input bf16; tensor cores, fp32 accumulation     */
+  KDTV_F32 = 0,      /* every input float32; computed on CUDA cores in fp32   */
+  KDTV_BF16 = 1,     /* every input bf16; tensor cores, fp32 accumulation     */
+  KDTV_BF16_FP8KV = 2 /* q_nope, q_rope, W_UK, W_UV bf16; the latent cache c_kv
+                        and k_rope one byte per element, OCP FP8 E4M3 (4-bit
+                        exponent with bias 7, 3-bit mantissa, no infinities,
+                        S.1111.111 = NaN), value = fp8 * kv_scale             */
 };
 
 enum kdtv_status {
@@ -93,7 +97,8 @@ typedef struct kdtv_dims {
   float scale;        /* softmax scale; <= 0 selects 1/sqrt(d_nope + d_rope)    */
   uint32_t flags;     /* KDTV_FLAG_*                                            */
   int32_t kv_chunk;   /* keys per split-KV chunk; 0 = chosen by the library     */
-  int32_t reserved;
+  float kv_scale;     /* KDTV_BF16_FP8KV: dequantisation scale of the cache;
+                         <= 0 selects 1.  Ignored for the other dtypes          */
   void* workspace;          /* device scratch, >= kdtv_workspace_size() bytes,
                                256-byte aligned, owned by the caller             */
   size_t workspace_bytes;

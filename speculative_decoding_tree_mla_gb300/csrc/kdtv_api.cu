@@ -30,7 +30,8 @@ int check_dims(const kdtv_dims* d) {
   if (d->B <= 0 || d->N <= 0 || d->H <= 0 || d->d_nope <= 0 || d->d_rope <= 0 ||
       d->d_v <= 0 || d->d_c <= 0)
     return KDTV_ERR_INVALID_ARG;
-  if (d->dtype != KDTV_F32 && d->dtype != KDTV_BF16) return KDTV_ERR_INVALID_ARG;
+  if (d->dtype != KDTV_F32 && d->dtype != KDTV_BF16 && d->dtype != KDTV_BF16_FP8KV)
+    return KDTV_ERR_INVALID_ARG;
   if (d->page_size < 0 || d->kv_chunk < 0) return KDTV_ERR_INVALID_ARG;
   if (d->page_size == 0) {
     if (d->t_stride < d->N) return KDTV_ERR_INVALID_ARG;
@@ -153,6 +154,7 @@ extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const vo
   a.page_size = d->page_size; a.t_stride = d->t_stride;
   a.max_pages = d->max_pages; a.num_pages = d->num_pages;
   a.scale = d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)(d->d_nope + d->d_rope));
+  a.kv_scale = (d->dtype == KDTV_BF16_FP8KV && d->kv_scale > 0.f) ? d->kv_scale : 1.0f;
   a.flags = d->flags;
   a.chunk = p.chunk; a.splits = p.splits;
   a.q_nope = q_nope; a.q_rope = q_rope; a.W_UK = W_UK; a.W_UV = W_UV;

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "kdtv.h"
@@ -51,6 +52,7 @@ struct Plan {
 struct Args {
   int B, N, H, d_nope, d_rope, d_v, d_c;
   int dtype;              // kdtv_dtype
+  float kv_scale;         // cache dequantisation scale (1 unless KDTV_BF16_FP8KV)
   int page_size, t_stride, max_pages, num_pages;
   float scale;
   unsigned int flags;
@@ -113,6 +115,7 @@ __device__ __forceinline__ PartialRef partials_of_row(const Args& a, long long r
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__nv_fp8_e4m3 x) { return static_cast<float>(x); }
 
 // Row of logical position t of request b in a cache tensor with `width`
 // elements per row; -1 if the page id is out of range.

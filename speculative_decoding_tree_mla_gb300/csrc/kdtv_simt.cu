@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kThreads) absorb_kernel(Args a) {
 }
 
 // One CTA: request b, node i, heads g0 .. g0+ng-1, keys of split s.
-template <typename T>
+// T: element type of q_rope; TC: element type of the cache (times kv_scale).
+template <typename T, typename TC>
 __global__ void __launch_bounds__(kThreads) attn_kernel(Args a, int G) {
   extern __shared__ float smem[];
   const int D = a.d_c + a.d_rope;
@@ -120,8 +121,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(Args a, int G) {
 #pragma unroll
   for (int j = 0; j < kMaxOutPerThread; ++j) o[j] = 0.f;
 
-  const T* ckv = static_cast<const T*>(a.c_kv);
-  const T* kr = static_cast<const T*>(a.k_rope);
+  const TC* ckv = static_cast<const TC*>(a.c_kv);
+  const TC* kr = static_cast<const TC*>(a.k_rope);
   __syncthreads();
 
   for (int t0 = k0; t0 < k1; t0 += kKeyTile) {
@@ -140,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(Args a, int G) {
       float x = 0.f;
       if (vis_s[kk]) {
         long long r = cache_row(a, b, t0 + kk);
-        x = d < a.d_c ? to_f32(ckv[r * a.d_c + d]) : to_f32(kr[r * a.d_rope + (d - a.d_c)]);
+        x = (d < a.d_c ? to_f32(ckv[r * a.d_c + d]) : to_f32(kr[r * a.d_rope + (d - a.d_c)])) *
+            a.kv_scale;
       }
       k_s[kk * Dp + d] = x;
     }
@@ -287,7 +289,7 @@ void launch_uproj_typed(const Args& a, cudaStream_t st) {
   uproj_kernel<T><<<grid_rows, kThreads, sm_up, st>>>(a);
 }
 
-template <typename T>
+template <typename T, typename TC>
 cudaError_t launch_typed(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t* ev) {
   launch_absorb_typed<T, float>(a, st);
   if (ev) cudaEventRecord(ev[1], st);
@@ -296,12 +298,12 @@ cudaError_t launch_typed(const Args& a, const Plan& p, cudaStream_t st, cudaEven
   const int D = a.d_c + a.d_rope;
   size_t sm_attn = sizeof(float) * ((size_t)G * D + (size_t)kKeyTile * (D + 1) +
                                     (size_t)G * kKeyTile + 3 * G);
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<T>,
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<T, TC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)sm_attn);
   if (e != cudaSuccess) return e;
   dim3 grid_attn(a.N * ((a.H + G - 1) / G), a.splits, a.B);
-  attn_kernel<T><<<grid_attn, kThreads, sm_attn, st>>>(a, G);
+  attn_kernel<T, TC><<<grid_attn, kThreads, sm_attn, st>>>(a, G);
   if (ev) cudaEventRecord(ev[2], st);
   return launch_combine_uproj(a, p, st, ev);
 }
@@ -309,7 +311,7 @@ cudaError_t launch_typed(const Args& a, const Plan& p, cudaStream_t st, cudaEven
 }  // namespace
 
 cudaError_t launch_absorb(const Args& a, cudaStream_t st, bool bf16_out) {
-  if (a.dtype == KDTV_BF16) {
+  if (a.dtype == KDTV_BF16 || a.dtype == KDTV_BF16_FP8KV) {
     if (bf16_out) launch_absorb_typed<__nv_bfloat16, __nv_bfloat16>(a, st);
     else launch_absorb_typed<__nv_bfloat16, float>(a, st);
   } else {
@@ -323,7 +325,7 @@ cudaError_t launch_combine_uproj(const Args& a, const Plan& p, cudaStream_t st,
   if (p.splits > 1024) return cudaErrorInvalidValue;
   combine_kernel<<<(unsigned)p.rows, 128, 0, st>>>(a);
   if (ev) cudaEventRecord(ev[3], st);
-  if (a.dtype == KDTV_BF16) launch_uproj_typed<__nv_bfloat16>(a, st);
+  if (a.dtype == KDTV_BF16 || a.dtype == KDTV_BF16_FP8KV) launch_uproj_typed<__nv_bfloat16>(a, st);
   else launch_uproj_typed<float>(a, st);
   if (ev) cudaEventRecord(ev[4], st);
   return cudaGetLastError();
@@ -332,8 +334,9 @@ cudaError_t launch_combine_uproj(const Args& a, const Plan& p, cudaStream_t st,
 cudaError_t launch_simt(const Args& a, const Plan& p, cudaStream_t s, cudaEvent_t* ev) {
   if (p.splits > 1024) return cudaErrorInvalidValue;
   if (p.heads_per_cta * a.d_c > kMaxOutPerThread * kThreads) return cudaErrorInvalidValue;
-  return a.dtype == KDTV_BF16 ? launch_typed<__nv_bfloat16>(a, p, s, ev)
-                              : launch_typed<float>(a, p, s, ev);
+  if (a.dtype == KDTV_BF16_FP8KV) return launch_typed<__nv_bfloat16, __nv_fp8_e4m3>(a, p, s, ev);
+  return a.dtype == KDTV_BF16 ? launch_typed<__nv_bfloat16, __nv_bfloat16>(a, p, s, ev)
+                              : launch_typed<float, float>(a, p, s, ev);
 }
 
 }  // namespace kdtv

@@ -14,7 +14,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkdtv.so")
 
-KDTV_F32, KDTV_BF16 = 0, 1
+KDTV_F32, KDTV_BF16, KDTV_BF16_FP8KV = 0, 1, 2
 KDTV_FLAG_SIMT = 0x1
 KDTV_FLAG_SIMT_PROJ = 0x2
 KDTV_FLAG_TEST_STALL = 0x100
@@ -38,7 +38,7 @@ class KdtvDims(ctypes.Structure):
         ("t_stride", ctypes.c_int32), ("max_pages", ctypes.c_int32),
         ("num_pages", ctypes.c_int32), ("scale", ctypes.c_float),
         ("flags", ctypes.c_uint32), ("kv_chunk", ctypes.c_int32),
-        ("reserved", ctypes.c_int32), ("workspace", ctypes.c_void_p),
+        ("kv_scale", ctypes.c_float), ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t), ("phase_events", ctypes.c_void_p),
     ]
 
@@ -89,13 +89,17 @@ def strerror(code):
     return lib().kdtv_strerror(int(code)).decode()
 
 
+DTYPE_CODE = {"f32": KDTV_F32, "bf16": KDTV_BF16, "fp8kv": KDTV_BF16_FP8KV}
+
+
 def make_dims(spec_or_shape, *, dtype, page_size=0, t_stride=0, max_pages=0,
-              num_pages=0, scale=0.0, flags=0, kv_chunk=0):
+              num_pages=0, scale=0.0, flags=0, kv_chunk=0, kv_scale=0.0):
     s = spec_or_shape
     d = KdtvDims()
     d.B, d.N, d.H = s.B, s.N, s.H
     d.d_nope, d.d_rope, d.d_v, d.d_c = s.d_nope, s.d_rope, s.d_v, s.d_c
-    d.dtype = KDTV_BF16 if dtype in ("bf16", KDTV_BF16) else KDTV_F32
+    d.dtype = DTYPE_CODE.get(dtype, dtype if isinstance(dtype, int) else KDTV_F32)
+    d.kv_scale = kv_scale
     d.page_size, d.t_stride = page_size, t_stride
     d.max_pages, d.num_pages = max_pages, num_pages
     d.scale, d.flags, d.kv_chunk = scale, flags, kv_chunk
@@ -130,7 +134,7 @@ class VerifyAttn:
     """
 
     def __init__(self, spec, tensors, *, t_stride=0, max_pages=0, num_pages=0,
-                 page_size=0, flags=0, kv_chunk=0, scale=0.0):
+                 page_size=0, flags=0, kv_chunk=0, scale=0.0, kv_scale=0.0):
         import torch
         self.torch = torch
         self.t = tensors
@@ -138,7 +142,7 @@ class VerifyAttn:
         self.dims = make_dims(spec, dtype=spec.dtype, page_size=page_size,
                               t_stride=t_stride, max_pages=max_pages,
                               num_pages=num_pages, scale=scale or spec.scale,
-                              flags=flags, kv_chunk=kv_chunk)
+                              flags=flags, kv_chunk=kv_chunk, kv_scale=kv_scale)
         nbytes = workspace_size(self.dims)
         if nbytes == 0:
             raise KdtvError(STATUS_CODE["KDTV_ERR_UNSUPPORTED"], "workspace size")
@@ -193,6 +197,7 @@ def for_workload(wl, device="cuda", **kw):
     if wl.page_size:
         names.append("page_table")
     tens = {n: wl.t[n].to(device).contiguous() for n in names}
+    kw.setdefault("kv_scale", wl.kv_scale)
     return VerifyAttn(wl.spec, tens, t_stride=wl.t_stride, max_pages=wl.max_pages,
                       num_pages=wl.num_pages, page_size=wl.page_size, **kw)
 

@@ -52,7 +52,7 @@ class Spec:
     d_rope: int
     d_v: int
     d_c: int
-    dtype: str                 # "f32" or "bf16"
+    dtype: str                 # "f32", "bf16" or "fp8kv" (bf16 q / weights, FP8 E4M3 cache)
     prefix: tuple              # ("fixed", L) | ("uniform", lo, hi) | ("loguniform", lo, hi)
     tree: tuple                # ("window", w or None, depth_cap) | ("chain",)
     paged: bool = False
@@ -148,6 +148,7 @@ class Workload:
     t_stride: int = 0
     max_pages: int = 0
     num_pages: int = 0
+    kv_scale: float = 0.0        # fp8kv: cache value = fp8 * kv_scale (0: not used)
 
     @property
     def page_size(self) -> int:
@@ -163,10 +164,48 @@ def _normal(rng, shape, std=1.0):
 
 def _as_dtype(x, dtype):
     t = torch.from_numpy(np.ascontiguousarray(x))
-    if dtype == "bf16":
+    if dtype in ("bf16", "fp8kv"):
         t = t.to(torch.bfloat16)
         return t, t.float().numpy()
     return t, x
+
+
+# ---- OCP FP8 E4M3 (storage format of the fp8kv cache) -------------------------------------
+# Byte S.EEEE.MMM: exponent bias 7; E = 0 holds subnormals M * 2^-9; E = 15 with
+# M = 7 is NaN; there are no infinities, so the largest value is 1.75 * 2^8 = 448.
+FP8_KV_SCALE = 0.125           # the fp8kv workloads store x / 0.125 and read fp8 * 0.125
+
+
+def fp8_e4m3_decode(codes):
+    """float32 values of E4M3 byte codes (uint8 array)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return (sign * mag).astype(np.float32)
+
+
+_E4M3_POS = fp8_e4m3_decode(np.arange(0x7F, dtype=np.uint8))   # codes 0x00 .. 0x7E, increasing
+
+
+def fp8_e4m3_encode(x):
+    """Nearest E4M3 byte code of each float32 (ties to the even code, saturating at
+    448), by search over the 127 non-negative finite values."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.minimum(np.abs(x), np.float32(448.0))
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    dl, dh = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick_hi = (dh < dl) | ((dh == dl) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)   # -0 for tiny negatives
+
+
+def _as_fp8_cache(x):
+    codes = fp8_e4m3_encode(x / np.float32(FP8_KV_SCALE))
+    return torch.from_numpy(codes), fp8_e4m3_decode(codes) * np.float32(FP8_KV_SCALE)
 
 
 def make(spec, *, parent=None, prefix_len=None, with_lm_head=False,
@@ -236,7 +275,12 @@ def make(spec, *, parent=None, prefix_len=None, with_lm_head=False,
 
     for name, arr in (("q_nope", q_nope), ("q_rope", q_rope), ("W_UK", W_UK),
                       ("W_UV", W_UV), ("c_kv", c_kv), ("k_rope", k_rope)):
-        wl.t[name], wl.f32[name] = _as_dtype(arr, spec.dtype)
+        if spec.dtype == "fp8kv" and name in ("c_kv", "k_rope"):
+            wl.t[name], wl.f32[name] = _as_fp8_cache(arr)
+        else:
+            wl.t[name], wl.f32[name] = _as_dtype(arr, spec.dtype)
+    if spec.dtype == "fp8kv":
+        wl.kv_scale = FP8_KV_SCALE
     wl.t["parent"] = torch.from_numpy(parent.copy())
     wl.t["prefix_len"] = torch.from_numpy(prefix_len.astype(np.int32))
     wl.f32["parent"], wl.f32["prefix_len"] = parent, prefix_len
