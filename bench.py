@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--config", default="kimi_single")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="tc", choices=["tc", "simt"])
+    ap.add_argument("--cache", default="native", choices=["native", "fp8"],
+                    help="fp8: the same workload with an FP8 E4M3 latent cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -91,9 +93,9 @@ def work(wl):
             2 * (s.d_c + s.d_rope) + 2 * s.d_c)
     absorb = 2 * s.B * s.N * s.H * s.d_nope * s.d_c
     uproj = 2 * s.B * s.N * s.H * s.d_c * s.d_v
-    esz = 2 if s.dtype == "bf16" else 4
+    esz = 2 if s.dtype in ("bf16", "fp8kv") else 4
     T = (np.asarray(f["prefix_len"]) + s.N).sum()
-    cache_bytes = int(T) * (s.d_c + s.d_rope) * esz
+    cache_bytes = int(T) * (s.d_c + s.d_rope) * (1 if s.dtype == "fp8kv" else esz)
     weights = s.H * s.d_c * (s.d_nope + s.d_v) * esz
     q = s.B * s.N * s.H * (s.d_nope + s.d_rope) * esz
     out = s.B * s.N * s.H * s.d_v * 4
@@ -309,7 +311,8 @@ def loop_steps(wl, dev, reps=200):
 def config_dict(wl):
     s = wl.spec
     f = wl.f32
-    return {"workload": s.name, "batch": s.B, "tree_nodes": s.N, "heads": s.H,
+    return {"workload": s.name + ("+fp8cache" if s.dtype == "fp8kv" else ""),
+            "batch": s.B, "tree_nodes": s.N, "heads": s.H,
             "d_nope": s.d_nope, "d_rope": s.d_rope, "d_v": s.d_v, "kv_lora": s.d_c,
             "prefix_len_mean": float(sum(int(x) for x in f["prefix_len"]) / s.B),
             "paged": s.paged, "seed": s.seed, "l2": "flushed (256 MiB write) before every call"}
@@ -323,7 +326,11 @@ def main():
     import torch
     from speculative_decoding_tree_mla_gb300 import workloads as W
     rank, ws, local = dist_init(args)
-    wl = W.make(args.config)
+    spec = W.SPECS[args.config]
+    if args.cache == "fp8":
+        import dataclasses
+        spec = dataclasses.replace(spec, dtype="fp8kv")
+    wl = W.make(spec)
     if args.impl == "reference":
         run_reference(args, wl, rank, ws)
         return
@@ -430,11 +437,13 @@ def main():
         line = {
             "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": ws, "steps": K,
             "warmup": Wm, "ms_per_step": mean_ms, "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": wl.spec.dtype,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32" if (op.dims.dtype != kdtv.KDTV_BF16 or flags) else "bf16",
             "data": "synthetic", "config": config_dict(wl),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tc,
                          "unit": "TFLOP/s", "frac": tflops / peak_tc,
-                         "traffic": attn_traffic(args.config),
+                         "traffic": (attn_traffic(args.config)
+                                     if not flags and args.cache == "native" else None),
                          "kernel": "attention (tree-masked scores, online softmax, P.c_kv)",
                          "peak_source": f"{pk_kind} bf16_tflops (burst)"},
             "call_roofline": {"t_roof_us": roof_us, "frac": roof_us / us_call,

@@ -275,6 +275,12 @@ extern "C" int kdtv_compact_kv(const kdtv_dims* d, void* c_kv, void* k_rope,
         d->N, d->d_c, d->d_rope, d->page_size, d->t_stride, d->max_pages, d->num_pages,
         static_cast<__nv_bfloat16*>(c_kv), static_cast<__nv_bfloat16*>(k_rope), prefix_len, path,
         path_len, page_table, status);
+  } else if (d->dtype == KDTV_BF16_FP8KV) {   // one-byte cache elements, moved as bytes
+    const size_t sm = sizeof(unsigned char) * kRowsChunk * W;
+    compact_kernel<unsigned char><<<d->B, kCompactThreads, sm, stream>>>(
+        d->N, d->d_c, d->d_rope, d->page_size, d->t_stride, d->max_pages, d->num_pages,
+        static_cast<unsigned char*>(c_kv), static_cast<unsigned char*>(k_rope), prefix_len, path,
+        path_len, page_table, status);
   } else if (d->dtype == KDTV_F32) {
     const size_t sm = sizeof(float) * kRowsChunk * W;
     compact_kernel<float><<<d->B, kCompactThreads, sm, stream>>>(

@@ -68,7 +68,7 @@ def _accepted_paths(rng, B, N):
     return paths, plen
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "fp8kv"])
 @pytest.mark.parametrize("paged", [False, True])
 def test_compact_kv_matches_oracle(dtype, paged):
     rng = np.random.default_rng(7)
@@ -91,8 +91,13 @@ def test_compact_kv_matches_oracle(dtype, paged):
                                      paths[b, :plen[b]].tolist(),
                                      page_table=wl.f32.get("page_table"),
                                      page_size=wl.page_size)
-    assert np.array_equal(c.float().cpu().numpy(), ref_c)
-    assert np.array_equal(k.float().cpu().numpy(), ref_k)
+    if dtype == "fp8kv":      # the cache holds E4M3 codes: compare the values they decode to
+        got_c = W.fp8_e4m3_decode(c.cpu().numpy()) * np.float32(wl.kv_scale)
+        got_k = W.fp8_e4m3_decode(k.cpu().numpy()) * np.float32(wl.kv_scale)
+    else:
+        got_c, got_k = c.float().cpu().numpy(), k.float().cpu().numpy()
+    assert np.array_equal(got_c, ref_c)
+    assert np.array_equal(got_k, ref_k)
 
 
 def test_compact_kv_rejects_bad_path():
