@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "kimi_single": ("9b3eea0d0592fc26da7c4f300da2204c0714999d0b3e8814dead95de923d8f22", 9594880),
-    "long": ("9b3eea0d0592fc26da7c4f300da2204c0714999d0b3e8814dead95de923d8f22", 1047564288),
+    "kimi_single": ("e50d127400e172edb4944829547b56d481d1622254e5e4ec52d8bd74c16df142", 9594624),
+    "long": ("e50d127400e172edb4944829547b56d481d1622254e5e4ec52d8bd74c16df142", 1040471040),
 }
 
 
