@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "kimi_single": ("e50d127400e172edb4944829547b56d481d1622254e5e4ec52d8bd74c16df142", 9594624),
-    "long": ("e50d127400e172edb4944829547b56d481d1622254e5e4ec52d8bd74c16df142", 1040471040),
+    "kimi_single": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 9594624),
+    "long": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 1041556480),
 }
 
 
@@ -454,7 +454,7 @@ def main():
             "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": ws, "steps": K,
             "warmup": Wm, "ms_per_step": mean_ms, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if (op.dims.dtype != kdtv.KDTV_BF16 or flags) else "bf16",
+            "dtype": "f32" if (op.dims.dtype == kdtv.KDTV_F32 or flags) else "bf16",
             "data": "synthetic", "config": config_dict(wl),
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tc,
                          "unit": "TFLOP/s", "frac": tflops / peak_tc,

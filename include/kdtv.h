@@ -52,7 +52,13 @@ enum kdtv_dtype {
   KDTV_BF16_FP8KV = 2 /* q_nope, q_rope, W_UK, W_UV bf16; the latent cache c_kv
                         and k_rope one byte per element, OCP FP8 E4M3 (4-bit
                         exponent with bias 7, 3-bit mantissa, no infinities,
-                        S.1111.111 = NaN), value = fp8 * kv_scale             */
+                        S.1111.111 = NaN), value = fp8 * kv_scale.  Tensor
+                        cores (the default where KDTV_BF16 has them): the
+                        rows a call reads are first widened exactly to bf16
+                        copies in the workspace (kdtv_workspace_size grows
+                        by 2 * (d_c + d_rope) bytes per cache row), rows past
+                        L_b + N in a request's last 64-key tile written as
+                        zeros; KDTV_FLAG_SIMT: fp32 on CUDA cores            */
 };
 
 enum kdtv_status {
@@ -70,8 +76,9 @@ enum kdtv_status {
 };
 
 /* kdtv_dims.flags */
-#define KDTV_FLAG_SIMT 0x1u          /* bf16 inputs on the CUDA-core path (the
-                                        tensor-core path is the default)          */
+#define KDTV_FLAG_SIMT 0x1u          /* bf16 / fp8-cache inputs on the CUDA-core
+                                        path (the tensor-core path is the
+                                        default)                                  */
 #define KDTV_FLAG_SIMT_PROJ 0x2u     /* bf16: tensor-core attention, but the absorb,
                                         split combine and up-projection on CUDA
                                         cores                                     */

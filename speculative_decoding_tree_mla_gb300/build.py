@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkdtv.so")
 SOURCES = ["kdtv_api.cu", "kdtv_simt.cu", "kdtv_tc.cu", "kdtv_tc_gemm.cu", "kdtv_next.cu",
-           "kdtv_noalloc.cu"]
+           "kdtv_noalloc.cu", "kdtv_fp8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

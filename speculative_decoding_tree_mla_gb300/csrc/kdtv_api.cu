@@ -46,8 +46,17 @@ int check_dims(const kdtv_dims* d) {
   return KDTV_OK;
 }
 
+// The dims the tensor-core kernels see: an fp8 cache is widened to bf16 first.
+kdtv_dims tc_view(const kdtv_dims* d) {
+  kdtv_dims v = *d;
+  if (v.dtype == KDTV_BF16_FP8KV) v.dtype = KDTV_BF16;
+  return v;
+}
+
 bool use_tensor_cores(const kdtv_dims* d) {
-  return d->dtype == KDTV_BF16 && !(d->flags & KDTV_FLAG_SIMT) && tc_supported(d);
+  if (d->dtype != KDTV_BF16 && d->dtype != KDTV_BF16_FP8KV) return false;
+  const kdtv_dims v = tc_view(d);
+  return !(d->flags & KDTV_FLAG_SIMT) && tc_supported(&v);
 }
 
 int make_plan(const kdtv_dims* d, Plan* p) {
@@ -91,6 +100,14 @@ int make_plan(const kdtv_dims* d, Plan* p) {
     p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
     p->off_sk = off;      off = align256(off + (size_t)(kSkHeader + 3 * R + clusters) * sizeof(int));
     p->off_anc = off;     off = align256(off + (size_t)d->B * d->N * 4 * sizeof(uint32_t));
+    if (d->dtype == KDTV_BF16_FP8KV) {
+      // bf16 copies of the fp8 cache, in the input's layout
+      const size_t kv_rows = d->page_size ? (size_t)d->num_pages * d->page_size
+                                          : (size_t)d->B * d->t_stride;
+      p->kv_widen = true;
+      p->off_kvc = off;   off = align256(off + kv_rows * d->d_c * sizeof(__nv_bfloat16));
+      p->off_kvr = off;   off = align256(off + kv_rows * d->d_rope * sizeof(__nv_bfloat16));
+    }
   } else {
     p->heads_per_cta = d->H < 16 ? d->H : 16;
     long long base = (long long)d->B * d->N * ((d->H + p->heads_per_cta - 1) / p->heads_per_cta);
@@ -127,7 +144,9 @@ extern "C" size_t kdtv_workspace_size(const kdtv_dims* d) {
 extern "C" int kdtv_launches_per_call(const kdtv_dims* d) {
   Plan p;
   if (make_plan(d, &p) != KDTV_OK) return -1;
-  return p.tensor_core ? tc_launches(d, p.splits) : 4;
+  if (!p.tensor_core) return 4;
+  const kdtv_dims v = tc_view(d);
+  return tc_launches(&v, p.splits) + (p.kv_widen ? 1 : 0);
 }
 
 extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const void* q_rope,
@@ -155,6 +174,7 @@ extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const vo
   a.max_pages = d->max_pages; a.num_pages = d->num_pages;
   a.scale = d->scale > 0.f ? d->scale : 1.0f / sqrtf((float)(d->d_nope + d->d_rope));
   a.kv_scale = (d->dtype == KDTV_BF16_FP8KV && d->kv_scale > 0.f) ? d->kv_scale : 1.0f;
+  a.o_scale = 1.0f;
   a.flags = d->flags;
   a.chunk = p.chunk; a.splits = p.splits;
   a.q_nope = q_nope; a.q_rope = q_rope; a.W_UK = W_UK; a.W_UV = W_UV;
@@ -181,6 +201,18 @@ extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const vo
   cudaEvent_t* ev = d->phase_events;
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return KDTV_ERR_CUDA;
   if (cudaMemsetAsync(ws, 0, kStatusBytes, stream) != cudaSuccess) return KDTV_ERR_CUDA;
+  if (p.kv_widen) {
+    // The bf16 kernels read exact bf16 copies of the fp8 values, written by
+    // a widening kernel ahead of the attention; kv_scale moves onto the
+    // scores and onto o_lat (both linear in the cache).
+    a.c_kv8 = a.c_kv;
+    a.k_rope8 = a.k_rope;
+    a.c_kv = ws + p.off_kvc;
+    a.k_rope = ws + p.off_kvr;
+    a.dtype = KDTV_BF16;
+    a.scale *= a.kv_scale;
+    a.o_scale = a.kv_scale;
+  }
   cudaError_t e = p.tensor_core ? launch_tc(a, p, stream, ev) : launch_simt(a, p, stream, ev);
   return e == cudaSuccess ? KDTV_OK : KDTV_ERR_CUDA;
 }

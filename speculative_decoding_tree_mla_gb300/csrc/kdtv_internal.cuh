@@ -45,7 +45,8 @@ struct Plan {
   int sms;                // streaming multiprocessors of the current device
   // tensor-core path (stream-K): CTA pairs, W bounds, partial slots
   int sk_clusters, sk_wmin, sk_wforce, rt_count, slots;
-  size_t off_qlat, off_part_o, off_part_ml, off_olat, off_sk, off_anc, total;
+  bool kv_widen;          // fp8 cache widened to bf16 copies at off_kvc / off_kvr
+  size_t off_qlat, off_part_o, off_part_ml, off_olat, off_sk, off_anc, off_kvc, off_kvr, total;
 };
 
 // Device-side view of the call (passed by value to kernels).
@@ -53,6 +54,8 @@ struct Args {
   int B, N, H, d_nope, d_rope, d_v, d_c;
   int dtype;              // kdtv_dtype
   float kv_scale;         // cache dequantisation scale (1 unless KDTV_BF16_FP8KV)
+  float o_scale;          // factor on each o_lat row in the combine (kv_scale when the
+                          // tensor-core path reads a widened, unscaled fp8 cache; else 1)
   int page_size, t_stride, max_pages, num_pages;
   float scale;
   unsigned int flags;
@@ -63,6 +66,8 @@ struct Args {
   const void* W_UV;
   const void* c_kv;
   const void* k_rope;
+  const void* c_kv8;      // fp8 cache widened into c_kv / k_rope before the attention
+  const void* k_rope8;    // (tensor-core path, KDTV_BF16_FP8KV), else nullptr
   const int32_t* parent;
   const int32_t* prefix_len;
   const int32_t* page_table;
@@ -215,6 +220,9 @@ cudaError_t launch_combine_uproj(const Args& a, const Plan& p, cudaStream_t s,
 cudaError_t launch_absorb_tc(const Args& a, cudaStream_t s, bool after_plan);
 cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t s,
                                     cudaEvent_t* ev);
+// fp8 cache (a.c_kv8, a.k_rope8) -> bf16 copies in the same layout (a.c_kv,
+// a.k_rope) of the rows the call reads
+cudaError_t launch_kv_widen(const Args& a, int sms, cudaStream_t s, bool pdl);
 bool absorb_tc_ok(const Args& a);
 bool combine_uproj_tc_ok(const Args& a);
 int tc_supported(const kdtv_dims* d);

@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(kThreads) attn_kernel(Args a, int G) {
   for (int g = tid; g < ng; g += blockDim.x) { ml[2 * g] = m_s[g]; ml[2 * g + 1] = l_s[g]; }
 }
 
-// o_lat[row] = sum_s e^{m_s - m*} o_s / sum_s e^{m_s - m*} l_s over the row's
-// partials (split-KV ranges, or the pieces of a stream-K plan).
+// o_lat[row] = o_scale * sum_s e^{m_s - m*} o_s / sum_s e^{m_s - m*} l_s over
+// the row's partials (split-KV ranges, or the pieces of a stream-K plan).
 __global__ void __launch_bounds__(128) combine_kernel(Args a) {
   const long long row = blockIdx.x;
   __shared__ float w_s[1024];
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(128) combine_kernel(Args a) {
       w_s[s] = w;
       l += w * ml[1];
     }
-    inv_l = l > 0.f ? 1.f / l : 0.f;
+    inv_l = l > 0.f ? a.o_scale / l : 0.f;
   }
   __syncthreads();
   for (int d = threadIdx.x; d < a.d_c; d += blockDim.x) {

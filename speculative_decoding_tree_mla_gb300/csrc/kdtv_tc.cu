@@ -1107,6 +1107,10 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
   e = simt_proj ? launch_absorb(a, st, /*bf16_out=*/true)
                 : launch_absorb_tc(a, st, /*after_plan=*/ev == nullptr);
   if (e != cudaSuccess) return e;
+  if (a.c_kv8) {   // fp8 cache: widen it beside the plan and absorb kernels
+    e = launch_kv_widen(a, p.sms, st, /*pdl=*/ev == nullptr);
+    if (e != cudaSuccess) return e;
+  }
   if (ev) cudaEventRecord(ev[1], st);
 
   TcCfg cfg;

@@ -222,7 +222,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
     }
 #pragma unroll
     for (int o = 1; o < kTpr; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const float inv = l > 0.f ? a.o_scale / l : 0.f;
     float* w = wts + r * UP_MAX_SPLITS;
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {

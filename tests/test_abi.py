@@ -57,6 +57,32 @@ def test_workspace_sizes(L, flags):
         assert kdtv.launches_per_call(d) > 0
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_fp8_cache_plan(L, paged):
+    """The tensor-core fp8 call is the bf16 call plus one launch that widens the
+    cache into the workspace (one bf16 copy of c_kv and k_rope in the input's
+    layout); the CUDA-core fp8 call keeps the bf16 CUDA-core plan."""
+    spec = W.SPECS["kimi_single"]
+    if paged:
+        kw = dict(page_size=64, max_pages=70, num_pages=300)
+        kv_rows = 300 * 64
+    else:
+        kw = dict(t_stride=4165)
+        kv_rows = spec.B * 4165
+    d16 = kdtv.make_dims(spec, dtype="bf16", **kw)
+    d8 = kdtv.make_dims(spec, dtype="fp8kv", kv_scale=0.125, **kw)
+    if kdtv.workspace_size(d16) == 0:
+        pytest.skip("tensor-core path not compiled in")
+    copies = kv_rows * (spec.d_c + spec.d_rope) * 2
+    assert kdtv.workspace_size(d16) + copies <= kdtv.workspace_size(d8) \
+        <= kdtv.workspace_size(d16) + copies + 512
+    assert kdtv.launches_per_call(d8) == kdtv.launches_per_call(d16) + 1
+    s16 = kdtv.make_dims(spec, dtype="bf16", flags=kdtv.KDTV_FLAG_SIMT, **kw)
+    s8 = kdtv.make_dims(spec, dtype="fp8kv", flags=kdtv.KDTV_FLAG_SIMT, **kw)
+    assert kdtv.workspace_size(s8) == kdtv.workspace_size(s16) > 0
+    assert kdtv.launches_per_call(s8) == kdtv.launches_per_call(s16) == 4
+
+
 @pytest.mark.parametrize("field,value,code", [
     ("N", 0, "KDTV_ERR_INVALID_ARG"),
     ("H", -1, "KDTV_ERR_INVALID_ARG"),
