@@ -173,6 +173,33 @@ def test_fp8_cache_scale_is_applied(flags, factor):
     _check(np.stack([a[0, 0], a[0, 7]]), ref, flags)
 
 
+@pytest.mark.parametrize("case", ["tree", "prefix", "page"])
+def test_fp8_tc_errors_reported_then_clean_call(case):
+    """A bad tree, prefix or page id in an fp8 call is reported through the
+    status word (the widening kernel skips what it cannot read), and the next
+    good call returns the same output as before."""
+    spec = W.small_spec("s_fp8_err", B=2, N=8, dtype="fp8kv", paged=case == "page",
+                        prefix=("fixed", 100), tree=("chain",))
+    wl = W.make(spec)
+    good, st = _run(wl)
+    assert st == 0
+    saved = {k: v.clone() for k, v in wl.t.items()}
+    if case == "tree":
+        wl.t["parent"][1, 5] = 7                    # parent after child
+        want = "KDTV_ERR_BAD_TREE"
+    elif case == "prefix":
+        wl.t["prefix_len"][1] = wl.t_stride         # L + N > t_stride
+        want = "KDTV_ERR_BAD_PREFIX"
+    else:
+        wl.t["page_table"][0, 1] = wl.num_pages + 5
+        want = "KDTV_ERR_BAD_PAGE"
+    _, st = _run(wl)
+    assert kdtv.STATUS[st] == want
+    wl.t.update(saved)
+    again, st = _run(wl)
+    assert st == 0 and np.array_equal(again, good)
+
+
 def test_unknown_dtype_rejected():
     """A dtype code outside the enum is refused on the host."""
     spec = W.small_spec("s_fp8_bad", B=1, N=4, dtype="fp8kv", prefix=("fixed", 64))
