@@ -211,6 +211,37 @@ def test_bf16_edge_cases(path, case):
     check(wl, got, all_nodes(wl))
 
 
+@pytest.mark.parametrize("path", list(PATH_IDS))
+@pytest.mark.parametrize("H,d_nope,d_v", [(128, 128, 128), (16, 192, 128), (32, 64, 64),
+                                          (8, 96, 192)])
+def test_bf16_head_layouts(path, H, d_nope, d_v):
+    """Head counts and head dims other than the Kimi layout, on the 512 + 64
+    latent cache: 128 heads (row tiles of one node), a 192-wide nope dim, and
+    head dims that the tensor-core absorb (d_nope % 64 != 0) or up-projection
+    (d_v != 128) kernels do not take, so the call mixes tensor-core attention
+    with CUDA-core projections."""
+    wl = small(f"heads_{H}_{d_nope}_{d_v}", B=2, N=12, H=H, d_nope=d_nope, d_v=d_v,
+               prefix=("uniform", 40, 400))
+    _skip_tc(PATH_IDS[path], wl)
+    got, st, _ = run(wl, flags=PATH_IDS[path])
+    assert st == 0
+    check(wl, got, all_nodes(wl))
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_tc_attention_with_simt_projections(paged):
+    """KDTV_FLAG_SIMT_PROJ: tensor-core attention between the CUDA-core absorb
+    (bf16 q_lat) and the CUDA-core combine + up-projection reading the
+    stream-K piece partials."""
+    wl = small("s_proj", B=3, N=16, paged=paged, prefix=("uniform", 50, 900))
+    _skip_tc(TC, wl)
+    a, st1, op = run(wl, flags=kdtv.KDTV_FLAG_SIMT_PROJ)
+    assert st1 == 0 and kdtv.launches_per_call(op.dims) == 5
+    check(wl, a, all_nodes(wl))
+    b, st2, _ = run(wl, flags=TC)
+    assert st2 == 0 and np.linalg.norm(a - b) / np.linalg.norm(b) <= BF16_REL
+
+
 # -- full-size workloads, sampled nodes -------------------------------------------
 @pytest.mark.parametrize("path", list(PATH_IDS))
 @pytest.mark.parametrize("name", ["kimi_single", "batched", "long", "paged"])
