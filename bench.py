@@ -42,6 +42,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 ATTN_TRAFFIC = {
     "kimi_single": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 9594624),
     "long": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 1041556480),
+    "batched": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 112783360),
+    "paged": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 2665444096),
 }
 
 
