@@ -40,10 +40,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "kimi_single": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 9594624),
-    "long": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 1041556480),
-    "batched": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 112783360),
-    "paged": ("7f8123f823323f8688e193f8424f7a44f811e3dfc3ffdc19ec800be535770013", 2665444096),
+    "kimi_single": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 9595136),
+    "long": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 1044246528),
+    "batched": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 136718080),
+    "paged": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 854387968),
 }
 
 

@@ -74,7 +74,8 @@ int make_plan(const kdtv_dims* d, Plan* p) {
   size_t off = kStatusBytes;
   if (p->tensor_core) {
     // Stream-K: one CTA pair per two SMs, each taking W consecutive 64-key
-    // units of the (request, row tile, key tile) sequence; W is at least
+    // units of the (row tile, key tile) sequence (row tiles lane-major:
+    // r = tile index * B + request); W is at least
     // wmin so that a row tile is cut into at most 63 pieces (the combine
     // kernel merges up to 64 partials per row).
     p->rt_count = (d->N * d->H + 127) / 128;

@@ -108,7 +108,7 @@ __device__ __forceinline__ PartialRef partials_of_row(const Args& a, long long r
   }
   const int nh = a.N * a.H;
   const int b = (int)(row / nh), rr = (int)(row % nh);
-  const int r = b * a.rt_count + rr / 128, tr = rr % 128;
+  const int r = (rr / 128) * a.B + b, tr = rr % 128;   // lane-major row tiles
   const int W = a.sk[1];
   const int* e = a.sk + kSkHeader + 3 * r;
   const int S = e[0], u = e[1], base = e[2];

@@ -8,8 +8,13 @@
 //
 // Work decomposition (stream-K).  Query rows are (node, head) pairs with the
 // head fastest, cut into 128-row tiles per request; the work of a row tile is
-// its sequence of 64-key tiles.  All (request, row tile, key tile) units form
-// one sequence and CTA pair c takes the W consecutive units [cW, (c+1)W),
+// its sequence of 64-key tiles.  Row tiles are ordered lane-major, r = rt * B
+// + b (tile index within the request first), so that the pairs that run side
+// by side hold the same tile index of neighbouring requests, or different
+// tiles of one request at nearby keys; a request's cache is then shared in
+// L2 by its row tiles instead of being swept once per tile.  All (row tile,
+// key tile) units form one sequence and CTA pair c takes the W consecutive
+// units [cW, (c+1)W),
 // split into pieces at row-tile boundaries; each piece writes one partial
 // (m, l, o_lat) that the combine kernel merges.  A small plan kernel computes
 // the unit offsets, W and the partial slots (and each request's ancestor
@@ -157,8 +162,8 @@ __device__ __forceinline__ const int* sk_row(const Args& a, int r) { return a.sk
 __device__ __forceinline__ void piece_fill(const Args& a, int r, int beg, int end, int W, Piece& p) {
   const int* e = sk_row(a, r);
   p.r = r;
-  p.b = r / a.rt_count;
-  p.rt = r - p.b * a.rt_count;
+  p.rt = r / a.B;
+  p.b = r - p.rt * a.B;
   p.t0 = beg - e[0];
   p.t1 = min(end, e[0] + e[1]) - e[0];
   p.slot = e[2] + (beg / W - e[0] / W);   // the first piece of r starts at S_r
@@ -975,10 +980,10 @@ __global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
     const int r = r0 + tid;
     int u = 0;
     if (r < R) {
-      const int b = r / a.rt_count;
+      const int b = r % a.B;                 // row tiles in lane-major order
       const int L = a.prefix_len[b];
       const bool ok = L >= 0 && (long long)L + a.N <= cap;
-      if (!ok && r % a.rt_count == 0) record_error(a.status, KDTV_ERR_BAD_PREFIX, (unsigned)b);
+      if (!ok && r < a.B) record_error(a.status, KDTV_ERR_BAD_PREFIX, (unsigned)b);
       u = ok ? (L + a.N + BN - 1) / BN : 0;
     }
     tmp[tid] = u;

@@ -1,7 +1,8 @@
 """The stream-K work plan's arithmetic, checked by enumeration on the host.
 
-The tensor-core attention splits the sequence of (request, row tile, 64-key
-tile) units into CTA-pair ranges [cW, (c+1)W) and cuts each range into pieces
+The tensor-core attention splits the sequence of (row tile, 64-key tile)
+units, row tiles in lane-major order r = tile index * B + request, into
+CTA-pair ranges [cW, (c+1)W) and cuts each range into pieces
 at row-tile boundaries.  The plan kernel and the combine kernels give the
 pieces of row tile r the partial slots base_r + (x / W - S_r / W), for a piece
 starting at unit x, with base_r = r + floor(S_r / W) and a count per row tile
@@ -56,7 +57,7 @@ def test_slots_are_distinct_bounded_and_counted(seed):
     wmin = max(1, -(-u_cap // 62))
     u_req = rng.integers(0, u_cap + 1, size=B)
     u_req[rng.random(B) < 0.1] = 0                      # invalid requests hold no units
-    u = np.repeat(u_req, rt_count).astype(np.int64)
+    u = np.tile(u_req, rt_count).astype(np.int64)     # lane-major: r = rt * B + b
     wforce = int(rng.integers(1, 40)) if seed % 3 == 0 else 0
     if wforce:   # the host launches enough pairs for a forced W
         pairs = max(pairs, -(-len(u) * u_cap // max(wforce, wmin)))
