@@ -40,10 +40,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "kimi_single": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 9595136),
-    "long": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 1044246528),
-    "batched": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 136718080),
-    "paged": ("69101fd49ff5e5401c2d50381751279e75e1bf6ed7f7c9b4d9cd547952c09dbe", 854387968),
+    "kimi_single": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 9598208),
+    "long": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 932646400),
+    "batched": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 131602944),
+    "paged": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 863827968),
 }
 
 

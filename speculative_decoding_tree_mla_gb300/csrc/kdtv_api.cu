@@ -99,7 +99,9 @@ int make_plan(const kdtv_dims* d, Plan* p) {
     p->off_part_o = off;  off = align256(off + (size_t)p->slots * 128 * d->d_c * sizeof(__nv_bfloat16));
     p->off_part_ml = off; off = align256(off + (size_t)p->slots * 128 * 2 * sizeof(float));
     p->off_olat = off;    off = align256(off + rows * d->d_c * sizeof(float));
-    p->off_sk = off;      off = align256(off + (size_t)(kSkHeader + 3 * R + clusters) * sizeof(int));
+    // header, {S, u, base} per row tile, first row tile per pair, then 8-int
+    // first-piece records per pair (16-byte aligned)
+    p->off_sk = off;      off = align256(off + (size_t)(kSkHeader + 3 * R + clusters + 3 + 8 * clusters) * sizeof(int));
     p->off_anc = off;     off = align256(off + (size_t)d->B * d->N * 4 * sizeof(uint32_t));
     if (d->dtype == KDTV_BF16_FP8KV) {
       // bf16 copies of the fp8 cache, in the input's layout

@@ -80,7 +80,8 @@ struct Args {
   float* o_lat;           // [rows, d_c]
   // Stream-K plan of the tensor-core attention (nullptr: split layout).
   int* sk;                // kSkHeader ints {U, W, clusters, R}, then {S_r, u_r, base_r} per row tile,
-                          // then the row tile of each CTA pair's first unit
+                          // then the row tile of each CTA pair's first unit, then (16-byte
+                          // aligned) 8 ints per pair: {r, S_r, u_r, base_r} of that tile, L_b
   uint32_t* anc_g;        // [B, N, 4] ancestor masks, written by the plan kernel
   int rt_count;           // 128-row tiles per request
   int sk_clusters;        // CTA pairs launched

@@ -170,14 +170,29 @@ __device__ __forceinline__ void piece_fill(const Args& a, int r, int beg, int en
   p.L = a.prefix_len[p.b];
 }
 
+// Offset (ints) in the plan of the per-pair first-piece records, 16-byte aligned.
+__host__ __device__ __forceinline__ int sk_rec_off(int R, int pairs) {
+  return (kSkHeader + 3 * R + pairs + 3) & ~3;
+}
+
 // First piece of CTA pair cl (unit range [beg, end)); false if the range is
-// empty.  The plan lists the row tile holding each pair's first unit.
+// empty.  The plan stores, per pair, the row tile holding its first unit with
+// that tile's {S, u, base} and prefix length, so one 32-byte load (beside the
+// header's) starts the pair.
 __device__ bool piece_first(const Args& a, int cl, int beg, int end, int W, Piece& p) {
   if (beg >= end) return false;
-  const int R = a.sk[3];
-  const int r = a.sk[kSkHeader + 3 * R + cl];
+  const int R = a.B * a.rt_count;
+  const int4* rec = reinterpret_cast<const int4*>(a.sk + sk_rec_off(R, a.sk_clusters)) + 2 * cl;
+  const int4 v0 = rec[0], v1 = rec[1];
+  const int r = v0.x;
   if (r < 0 || r >= R) return false;
-  piece_fill(a, r, beg, end, W, p);
+  p.r = r;
+  p.rt = r / a.B;
+  p.b = r - p.rt * a.B;
+  p.t0 = beg - v0.y;
+  p.t1 = min(end, v0.y + v0.z) - v0.y;
+  p.slot = v0.w + (beg / W - v0.y / W);
+  p.L = v1.x;
   return true;
 }
 
@@ -1021,6 +1036,19 @@ __global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
     e[3 * r + 2] = r + S / W;
     const long long c_end = ((long long)S + u + W - 1) / W;
     for (long long c = ((long long)S + W - 1) / W; c < c_end && c < npair; ++c) first[c] = r;
+  }
+  __syncthreads();
+  // per-pair first-piece records {r, S_r, u_r, base_r}, {L_b, 0, 0, 0}
+  int4* rec = reinterpret_cast<int4*>(a.sk + sk_rec_off(R, npair));
+  for (int c = tid; c < npair; c += 256) {
+    const int r = first[c];
+    int4 v0 = make_int4(r, 0, 0, 0), v1 = make_int4(0, 0, 0, 0);
+    if (r < R) {
+      v0.y = e[3 * r]; v0.z = e[3 * r + 1]; v0.w = e[3 * r + 2];
+      v1.x = a.prefix_len[r % a.B];
+    }
+    rec[2 * c] = v0;
+    rec[2 * c + 1] = v1;
   }
   if (tid == 0) {
     a.sk[0] = U;
