@@ -97,3 +97,46 @@ def test_single_request_kimi_shape():
     assert sum(1 for *_, x, e in ps) == 32 + sum(1 for r in range(32)
                                                  for m in range(1, 200)
                                                  if S[r] < m * W < S[r] + 65)
+
+
+def first_piece_from_record(rec, beg, end, W):
+    """A pair's first piece as the attention kernel derives it from the pair's
+    plan record {r, S_r, u_r, base_r} alone: (r, first unit, end unit, slot)."""
+    r, S_r, u_r, base_r = rec
+    return r, beg, min(end, S_r + u_r), base_r + (beg // W - S_r // W)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_first_piece_records_match_enumeration(seed):
+    """The per-pair plan record (the row tile holding unit cW with that tile's
+    S, u and base) gives the same first piece and slot as walking the pair's
+    range, for every pair with work; pairs without work have no record."""
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 30))
+    rt_count = int(rng.integers(1, 9))
+    pairs = int(rng.integers(1, 80))
+    u_cap = int(rng.integers(1, 300))
+    wmin = max(1, -(-u_cap // 62))
+    u_req = rng.integers(0, u_cap + 1, size=B)
+    u_req[rng.random(B) < 0.15] = 0
+    u = np.tile(u_req, rt_count).astype(np.int64)
+    S, U, W, base = plan(u, pairs, wmin)
+    R = len(u)
+    # the plan kernel's records: first[c] = the row tile holding unit cW
+    first = [R] * pairs
+    for r in range(R):
+        c_beg, c_end = -(-int(S[r]) // W), -(-(int(S[r]) + int(u[r])) // W)
+        for c in range(c_beg, min(c_end, pairs)):
+            first[c] = r
+    ps = pieces(u, S, U, W, pairs)
+    for c in range(pairs):
+        beg, end = c * W, min((c + 1) * W, U)
+        mine = [p for p in ps if p[0] == c]
+        if beg >= end:
+            assert not mine
+            continue
+        r = first[c]
+        assert r < R
+        got = first_piece_from_record((r, int(S[r]), int(u[r]), int(base[r])), beg, end, W)
+        _, r0, x0, e0 = mine[0]
+        assert got == (r0, x0, e0, int(base[r0] + (x0 // W - S[r0] // W)))
