@@ -1,0 +1,121 @@
+"""The device-built stream-K plan and ancestor masks, bit for bit.
+
+After a tensor-core call the workspace holds what `sk_plan_kernel` wrote:
+* the plan table: the header {U, W, pairs, R}; {S_r, u_r, base_r} per row tile
+  (row tiles lane-major, r = tile index * B + request); the row tile holding
+  each pair's first unit; one 8-int record per pair {r, S_r, u_r, base_r, L_b};
+* the ancestor masks [B, N, 4] u32 (bit j of node i's mask set iff j lies on
+  i's root path, i included).
+
+Both are integer results with one correct value, so they are compared exactly
+with a host model written from the same definitions: units per row tile
+ceil((L_b + N) / 64) (0 for an invalid prefix), W = max(ceil(U / pairs),
+ceil(u_cap / 62)), base_r = r + floor(S_r / W), and the root paths of
+parent[].  The plan and the masks are the last two workspace regions of a
+bf16 tensor-core call, each 256-byte aligned.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_tree_mla_gb300 import kdtv, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_decoding_tree_mla_gb300 import build
+    build.build()
+
+
+def a256(x):
+    return (x + 255) // 256 * 256
+
+
+def host_plan(wl, pairs):
+    s = wl.spec
+    B, N, H = s.B, s.N, s.H
+    rt = -(-(N * H) // 128)
+    R = B * rt
+    t_cap = wl.max_pages * 64 if wl.page_size else wl.t_stride
+    L = np.asarray(wl.f32["prefix_len"], dtype=np.int64)
+    ok = (L >= 0) & (L + N <= t_cap)
+    u_req = np.where(ok, -(-(L + N) // 64), 0)
+    u = np.tile(u_req, rt)                      # r = tile index * B + request
+    S = np.concatenate([[0], np.cumsum(u)[:-1]])
+    U = int(u.sum())
+    wmin = max(1, -(-(-(-t_cap // 64)) // 62))
+    Wd = max(-(-U // pairs), wmin, 1)
+    base = np.arange(R) + S // Wd
+    first = np.full(pairs, R, dtype=np.int64)
+    for r in range(R):
+        for c in range(-(-int(S[r]) // Wd), min(-(-(int(S[r]) + int(u[r])) // Wd), pairs)):
+            first[c] = r
+    rec = np.zeros((pairs, 8), dtype=np.int64)
+    for c in range(pairs):
+        r = int(first[c])
+        rec[c, 0] = r
+        if r < R:
+            rec[c, 1:4] = S[r], u[r], base[r]
+            rec[c, 4] = L[r % B]
+    return dict(U=U, W=Wd, R=R, S=S, u=u, base=base, first=first, rec=rec)
+
+
+def host_masks(parent):
+    B, N = parent.shape
+    m = np.zeros((B, N, 4), dtype=np.uint32)
+    for b in range(B):
+        for i in range(N):
+            j = i
+            while True:
+                m[b, i, j >> 5] |= np.uint32(1 << (j & 31))
+                if j == 0:
+                    break
+                j = int(parent[b, j])
+    return m
+
+
+CASES = {
+    "ragged": lambda: W.make(W.small_spec("plan_r", B=3, N=16, prefix=("uniform", 30, 1500))),
+    "paged": lambda: W.make(W.small_spec("plan_p", B=5, N=8, paged=True,
+                                         prefix=("loguniform", 40, 900))),
+    "batched": lambda: W.make("batched"),
+    "kimi_single": lambda: W.make("kimi_single"),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES) + ["bad_prefix"])
+def test_device_plan_and_masks_match_host_model(case):
+    wl = CASES["ragged"]() if case == "bad_prefix" else CASES[case]()
+    if case == "bad_prefix":
+        wl.t["prefix_len"][1] = wl.t_stride      # request 1 holds no units
+        wl.f32["prefix_len"] = wl.t["prefix_len"].numpy().astype(np.int64)
+    op = kdtv.for_workload(wl, "cuda")
+    if kdtv.workspace_size(op.dims) == 0:
+        pytest.skip("tensor-core path not compiled in")
+    op.workspace.zero_()
+    op()
+    st = op.status()
+    assert kdtv.STATUS[st] == ("KDTV_ERR_BAD_PREFIX" if case == "bad_prefix" else "KDTV_OK")
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    hp = host_plan(wl, pairs)
+    B, N, R = wl.spec.B, wl.spec.N, hp["R"]
+    ws = op.workspace.cpu().numpy()
+    sk_ints = 4 + 3 * R + pairs + 3 + 8 * pairs
+    off_anc = ws.size - a256(B * N * 16)
+    off_sk = off_anc - a256(sk_ints * 4)
+    sk = ws[off_sk: off_sk + sk_ints * 4].view(np.int32).astype(np.int64)
+    assert sk[:4].tolist() == [hp["U"], hp["W"], pairs, R]
+    e = sk[4: 4 + 3 * R].reshape(R, 3)
+    assert np.array_equal(e[:, 0], hp["S"]) and np.array_equal(e[:, 1], hp["u"])
+    assert np.array_equal(e[:, 2], hp["base"])
+    assert np.array_equal(sk[4 + 3 * R: 4 + 3 * R + pairs], hp["first"])
+    rec_off = (4 + 3 * R + pairs + 3) & ~3
+    rec = sk[rec_off: rec_off + 8 * pairs].reshape(pairs, 8)
+    assert np.array_equal(rec, hp["rec"])
+    anc = ws[off_anc: off_anc + B * N * 16].view(np.uint32).reshape(B, N, 4)
+    assert np.array_equal(anc, host_masks(wl.f32["parent"]))
