@@ -123,15 +123,18 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(
 // ---- best-first tree build ----------------------------------------------------------------
 // One warp per request.  Candidate child k of node u (slot u K + k) is one
 // 64-bit word whose unsigned order is the preference order: the score's
-// order-preserving bits in the high half (higher score first), ~key in the
-// low half (key = u 65536 + k, so a lower parent and then a lower k win
-// ties); 0 is a taken or absent child.  Each node also keeps the word of its
-// best remaining child, so a step is:
-//   * a warp-wide maximum over the n node words (two 32-bit reductions: the
+// order-preserving bits in the high half (higher score first); in the low
+// half, (2^25 - 1 - (64 u + k)) << 7 (a lower parent and then a lower k win
+// ties) with the parent's depth in the low 7 bits (N <= 128, K <= 64 and the
+// depths used are below 128, so the key is unique and the depth never decides
+// the order); 0 is a taken or absent child.  Each node keeps the word of its
+// best remaining child in a register of lane (node % 32), so a step is:
+//   * a warp-wide maximum over the node words (two 32-bit reductions: the
 //     high half, then the low half among the lanes holding the highest);
 //   * the winner becomes node n;
 //   * the lanes recompute the best remaining child of the winner's parent and
-//     the best child of the new node (K children each, one per lane).
+//     the best child of the new node (K children each, one per lane), and the
+//     two owning lanes update their registers.
 // The proposals of the depths a tree can reach (min(D, N - 1)) are staged in
 // shared memory first; the nodes are written out at the end.
 constexpr int kBuildThreads = 32;
@@ -143,8 +146,21 @@ __device__ __forceinline__ uint32_t order_bits(float x) {
 __device__ __forceinline__ float from_order_bits(uint32_t o) {
   return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
 }
-__device__ __forceinline__ unsigned long long cand_word(float s, int key) {
-  return ((unsigned long long)order_bits(s) << 32) | (uint32_t)~(uint32_t)key;
+__device__ __forceinline__ unsigned long long cand_word(float s, int u, int k, int parent_depth) {
+  const uint32_t key = 0x1ffffffu - (uint32_t)(u * 64 + k);
+  return ((unsigned long long)order_bits(s) << 32) | (key << 7) | (uint32_t)parent_depth;
+}
+// This lane's node words (nodes lane, lane + 32, lane + 64, lane + 96): set
+// the one of node x to w if this lane owns it.
+__device__ __forceinline__ void set_node_word(unsigned long long& n0, unsigned long long& n1,
+                                              unsigned long long& n2, unsigned long long& n3,
+                                              int x, int lane, unsigned long long w) {
+  const bool mine = (x & 31) == lane;
+  const int j = x >> 5;
+  n0 = (mine && j == 0) ? w : n0;
+  n1 = (mine && j == 1) ? w : n1;
+  n2 = (mine && j == 2) ? w : n2;
+  n3 = (mine && j == 3) ? w : n3;
 }
 // Maximum of a 64-bit word over the warp.
 __device__ __forceinline__ unsigned long long warp_max_word(unsigned long long w) {
@@ -161,8 +177,7 @@ __global__ void __launch_bounds__(kBuildThreads) tree_build_kernel(
   extern __shared__ __align__(16) unsigned char sbuf[];
   const int Ds = D < N - 1 ? D : N - 1;                      // depths whose proposals are used
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(sbuf);   // [N*K]
-  unsigned long long* nbest = cand + N * K;                 // [N] best remaining child per node
-  int* ndepth = reinterpret_cast<int*>(nbest + N);          // [N]
+  int* ndepth = reinterpret_cast<int*>(cand + N * K + N);   // [N]
   float* lps = reinterpret_cast<float*>(ndepth + N);        // [Ds*K] staged log-probabilities
   int* tks = reinterpret_cast<int*>(lps + Ds * K);          // [Ds*K] staged tokens
   int* opar = tks + Ds * K;                                 // [N] outputs, written out at the end
@@ -175,18 +190,19 @@ __global__ void __launch_bounds__(kBuildThreads) tree_build_kernel(
 #pragma unroll 4
   for (int i = lane; i < Ds * K; i += 32) { lps[i] = lp[i]; tks[i] = tk[i]; }
   __syncwarp();
+  unsigned long long nb0 = 0ull, nb1 = 0ull, nb2 = 0ull, nb3 = 0ull;   // nodes lane, lane + 32, ...
   // the root and its children
   {
     unsigned long long m = 0ull;
     if (Ds > 0)
       for (int k = lane; k < K; k += 32) {
-        const unsigned long long w = cand_word(__fadd_rn(0.f, lps[k]), k);
+        const unsigned long long w = cand_word(__fadd_rn(0.f, lps[k]), 0, k, 0);
         cand[k] = w;
         m = max(m, w);
       }
     m = warp_max_word(m);
     if (lane == 0) {
-      nbest[0] = m;
+      nb0 = m;
       opar[0] = -1; otok[0] = root_token[b]; osco[0] = 0.f;
       ndepth[0] = 0;
     }
@@ -194,14 +210,13 @@ __global__ void __launch_bounds__(kBuildThreads) tree_build_kernel(
   __syncwarp();
   int n = 1;
   while (n < N) {
-    unsigned long long m = 0ull;
-    for (int i = lane; i < n; i += 32) m = max(m, nbest[i]);
-    const unsigned long long win = warp_max_word(m);
+    const unsigned long long win = warp_max_word(max(max(nb0, nb1), max(nb2, nb3)));
     if (win == 0ull) break;                       // frontier empty
     const float sw = from_order_bits((uint32_t)(win >> 32));
-    const int key = (int)~(uint32_t)win;
-    const int u = key >> 16, k = key & 0xffff;
-    const int d = ndepth[u];
+    const uint32_t low = (uint32_t)win;
+    const int d = (int)(low & 127u);              // the parent's depth
+    const int key = (int)(0x1ffffffu - (low >> 7));
+    const int u = key >> 6, k = key & 63;
     const bool grow = d + 1 < Ds;
     // the parent's remaining children, and the new node's children
     unsigned long long mu = 0ull, mn = 0ull;
@@ -210,16 +225,16 @@ __global__ void __launch_bounds__(kBuildThreads) tree_build_kernel(
       if (kk == k) { wu = 0ull; cand[u * K + kk] = 0ull; }   // taken
       mu = max(mu, wu);
       if (grow) {
-        const unsigned long long wn = cand_word(__fadd_rn(sw, lps[(d + 1) * K + kk]), n * 65536 + kk);
+        const unsigned long long wn = cand_word(__fadd_rn(sw, lps[(d + 1) * K + kk]), n, kk, d + 1);
         cand[n * K + kk] = wn;
         mn = max(mn, wn);
       }
     }
     mu = warp_max_word(mu);
     mn = warp_max_word(mn);
+    set_node_word(nb0, nb1, nb2, nb3, u, lane, mu);
+    set_node_word(nb0, nb1, nb2, nb3, n, lane, mn);
     if (lane == 0) {
-      nbest[u] = mu;
-      nbest[n] = mn;
       opar[n] = u; otok[n] = tks[d * K + k]; osco[n] = sw;
       ndepth[n] = d + 1;
     }
