@@ -1,6 +1,7 @@
 """Pins for the oracles of the loop steps around the verify attention
 (tree accept, KV compaction, best-first tree build); CPU only."""
 
+import heapq
 import itertools
 import json
 import os
@@ -203,3 +204,162 @@ def test_build_matches_brute_force_top_n(seed):
         p = t["parent"][i]
         assert p < i and t["depth"][i] == t["depth"][p] + 1
         assert t["score"][i] == np.float32(t["score"][p] + lp[t["depth"][p], ranks[i][-1]])
+
+
+def test_build_equal_scores_is_level_order_in_rank_order():
+    """All proposals equally likely: every candidate at depth d scores d times
+    the same value, so best-first with the stated tie rule (lower parent, then
+    lower k) lays the complete K-ary tree out level by level, each node's
+    children in rank order."""
+    D, K = 3, 3
+    lp = np.full((D, K), -0.25, np.float32)
+    tok = np.arange(D * K).reshape(D, K) + 50
+    n = 1 + K + K * K + K ** 3
+    t = TS.tree_build(lp, tok, 9, n)
+    want_parent, want_tok, frontier = [-1], [9], [0]
+    for d in range(D):
+        nxt = []
+        for u in frontier:
+            for k in range(K):
+                want_parent.append(u)
+                want_tok.append(int(tok[d, k]))
+                nxt.append(len(want_parent) - 1)
+        frontier = nxt
+    assert t["parent"].tolist() == want_parent
+    assert t["token"].tolist() == want_tok
+    # one fewer node cuts the last level short at its highest parent / rank
+    t2 = TS.tree_build(lp, tok, 9, n - 1)
+    assert t2["parent"].tolist() == want_parent[:-1]
+
+
+# -- planted mistakes: each must be caught by one of the pins above ------------------------
+def _accept_highest_child(parent_b, draft_tok_b, target_argmax_b):
+    parent_b = [int(p) for p in parent_b]
+    path, u = [0], 0
+    while True:
+        kids = [c for c in range(1, len(parent_b)) if parent_b[c] == u
+                and int(draft_tok_b[c]) == int(target_argmax_b[u])]
+        if not kids:
+            break
+        u = kids[-1]
+        path.append(u)
+    return path, int(target_argmax_b[u])
+
+
+def _accept_child_own_argmax(parent_b, draft_tok_b, target_argmax_b):
+    parent_b = [int(p) for p in parent_b]
+    path, u = [0], 0
+    while True:
+        kids = [c for c in range(1, len(parent_b)) if parent_b[c] == u
+                and int(draft_tok_b[c]) == int(target_argmax_b[c])]
+        if not kids:
+            break
+        u = kids[0]
+        path.append(u)
+    return path, int(target_argmax_b[u])
+
+
+def _accept_bonus_from_root(parent_b, draft_tok_b, target_argmax_b):
+    path, _ = ORIG_TS["tree_accept"](parent_b, draft_tok_b, target_argmax_b)
+    return path, int(target_argmax_b[0])
+
+
+def _accept_first_child_only(parent_b, draft_tok_b, target_argmax_b):
+    parent_b = [int(p) for p in parent_b]
+    path, u = [0], 0
+    while True:
+        kids = [c for c in range(1, len(parent_b)) if parent_b[c] == u]
+        if not kids or int(draft_tok_b[kids[0]]) != int(target_argmax_b[u]):
+            break
+        u = kids[0]
+        path.append(u)
+    return path, int(target_argmax_b[u])
+
+
+def _compact_dst_shifted(c_kv, k_rope, b, L, path, page_table=None, page_size=0):
+    return ORIG_TS["compact_kv"](c_kv, k_rope, b, L + 1, [p - 1 if p else 0 for p in path],
+                                 page_table, page_size)
+
+
+def _compact_paged_ignores_table(c_kv, k_rope, b, L, path, page_table=None, page_size=0):
+    if not page_size:
+        return ORIG_TS["compact_kv"](c_kv, k_rope, b, L, path)
+    c_new, k_new = np.array(c_kv, copy=True), np.array(k_rope, copy=True)
+    for k, a in enumerate(path):
+        s, d = L + int(a), L + k
+        c_new[d // page_size, d % page_size] = c_kv[s // page_size, s % page_size]
+        k_new[d // page_size, d % page_size] = k_rope[s // page_size, s % page_size]
+    return c_new, k_new
+
+
+def _build_worst_first(logp, tokens, root_token, n_nodes):
+    return ORIG_TS["tree_build"](-np.asarray(logp, np.float32), tokens, root_token, n_nodes)
+
+
+def _build_ties_high_parent(logp, tokens, root_token, n_nodes):
+    logp = np.asarray(logp, np.float32)
+    D, K = logp.shape
+    parent, token, depth, score = [-1], [int(root_token)], [0], [np.float32(0.0)]
+    heap = []
+
+    def push(u):
+        if depth[u] < D:
+            for k in range(K):
+                s = np.float32(score[u] + logp[depth[u], k])
+                heapq.heappush(heap, (-float(s), -u, k, s))
+    push(0)
+    while heap and len(parent) < n_nodes:
+        _, mu, k, s = heapq.heappop(heap)
+        u = -mu
+        parent.append(u)
+        token.append(int(tokens[depth[u], k]))
+        depth.append(depth[u] + 1)
+        score.append(s)
+        push(len(parent) - 1)
+    return {"parent": np.asarray(parent, np.int32), "token": np.asarray(token, np.int32),
+            "depth": np.asarray(depth, np.int32), "score": np.asarray(score, np.float32)}
+
+
+def _build_depth_short(logp, tokens, root_token, n_nodes):
+    return ORIG_TS["tree_build"](np.asarray(logp)[:-1], np.asarray(tokens)[:-1], root_token,
+                                 n_nodes)
+
+
+ORIG_TS = {n: getattr(TS, n) for n in ("tree_accept", "compact_kv", "tree_build")}
+
+_ACCEPT_PINS = [test_accept_reproduces_printed_run, test_accept_stops_at_sentinel,
+                test_accept_duplicate_siblings_take_lowest_index] + \
+    [lambda s=s: test_accept_is_longest_valid_path(s) for s in range(12)]
+_COMPACT_PINS = [test_compact_identity_on_chain_prefix, test_compact_paged_equals_contiguous] + \
+    [lambda s=s: test_compact_moves_rows_and_nothing_else(s) for s in range(6)]
+_BUILD_PINS = [test_build_k1_is_chain, test_build_depth1_is_star_in_rank_order,
+               test_build_equal_scores_is_level_order_in_rank_order] + \
+    [lambda s=s: test_build_matches_brute_force_top_n(s) for s in range(8)]
+
+TREE_STEP_MUTATIONS = {
+    "accept_takes_highest_matching_child": ("tree_accept", _accept_highest_child, _ACCEPT_PINS),
+    "accept_compares_child_own_argmax": ("tree_accept", _accept_child_own_argmax, _ACCEPT_PINS),
+    "accept_bonus_from_root": ("tree_accept", _accept_bonus_from_root, _ACCEPT_PINS),
+    "accept_first_child_only": ("tree_accept", _accept_first_child_only, _ACCEPT_PINS),
+    "compact_destination_shifted": ("compact_kv", _compact_dst_shifted, _COMPACT_PINS),
+    "compact_paged_ignores_page_table": ("compact_kv", _compact_paged_ignores_table, _COMPACT_PINS),
+    "build_worst_first": ("tree_build", _build_worst_first, _BUILD_PINS),
+    "build_ties_to_higher_parent": ("tree_build", _build_ties_high_parent, _BUILD_PINS),
+    "build_one_depth_short": ("tree_build", _build_depth_short, _BUILD_PINS),
+}
+
+
+@pytest.mark.parametrize("mutation", list(TREE_STEP_MUTATIONS))
+def test_tree_step_pins_catch_planted_mistake(mutation, monkeypatch):
+    attr, fn, pins = TREE_STEP_MUTATIONS[mutation]
+    monkeypatch.setattr(TS, attr, fn)
+    caught = False
+    for pin in pins:
+        try:
+            pin()
+        except pytest.skip.Exception:
+            continue
+        except AssertionError:
+            caught = True
+            break
+    assert caught, f"no pin caught mutation {mutation}"
