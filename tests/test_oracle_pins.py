@@ -125,11 +125,12 @@ def _m_up_sum_heads(o, Wv):
     return np.einsum("hvd,gd->hv", np.asarray(Wv, np.float64), np.asarray(o, np.float64))
 
 
-def _m_paged_swap(c_kv, k_rope, b, positions, page_table=None, page_size=0):
+def _m_paged_ignores_table(c_kv, k_rope, b, positions, page_table=None, page_size=0):
     if page_size:
         positions = np.asarray(positions, np.int64)
-        pages = np.asarray(page_table)[b, positions % page_size]
-        slots = positions // page_size % page_size
+        pages = b * (np.asarray(page_table).shape[1]) + positions // page_size
+        pages = np.minimum(pages, c_kv.shape[0] - 1)
+        slots = positions % page_size
         return np.asarray(c_kv[pages, slots], np.float64), np.asarray(k_rope[pages, slots], np.float64)
     return ORIG["gather_cache"](c_kv, k_rope, b, positions, page_table, page_size)
 
@@ -147,7 +148,7 @@ MUTATIONS = {
     "mask_drops_root": ("ancestor_path", _m_root_missing),
     "softmax_over_heads": ("softmax_rows", _m_softmax_heads),
     "up_project_sums_heads": ("up_project", _m_up_sum_heads),
-    "paged_page_slot_swapped": ("gather_cache", _m_paged_swap),
+    "paged_ignores_page_table": ("gather_cache", _m_paged_ignores_table),
 }
 
 
@@ -159,7 +160,7 @@ def test_pins_catch_planted_mistake(mutation, monkeypatch):
     for name, pin in P.all_pins().items():
         try:
             worst = max(worst, pin())
-        except Exception:
+        except AssertionError:
             worst = float("inf")
         if worst > 1e-6:
             break
