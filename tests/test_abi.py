@@ -157,3 +157,55 @@ def test_next_steps_reject_bad_args_on_host(L):
     d = _dims()
     assert kdtv.STATUS[L.kdtv_compact_kv(ctypes.byref(d), fake, fake, fake, fake, fake, None, None, None)] == "KDTV_ERR_INVALID_ARG"
     assert kdtv.STATUS[L.kdtv_compact_kv(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, None)] == "KDTV_ERR_INVALID_ARG"
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """A C11 program (gcc, -pedantic -Werror) includes kdtv.h, takes the address
+    of every declared entry point, links against the library and calls the
+    host-only parts: the boundary needs no C++ or Python on the caller's side."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = None
+    for root in (os.environ.get("CUDA_HOME"), "/usr/local/cuda"):
+        if root and os.path.exists(os.path.join(root, "include", "cuda_runtime_api.h")):
+            cuda_inc = os.path.join(root, "include")
+            break
+    if not cc or not cuda_inc:
+        pytest.skip("no C compiler or CUDA headers")
+    names = header_functions()
+    lib_dir = os.path.dirname(kdtv.lib()._name)
+    src = tmp_path / "caller.c"
+    src.write_text("\n".join([
+        '#include "kdtv.h"',
+        "#include <stdio.h>",
+        "#include <string.h>",
+        "typedef void (*entry_fn)(void);",
+        "static const entry_fn entries[] = {" + ", ".join(f"(entry_fn){n}" for n in names) + "};",
+        "int main(void) {",
+        "  kdtv_dims d;",
+        "  memset(&d, 0, sizeof d);",
+        "  d.B = 1; d.N = 16; d.H = 4; d.d_nope = 32; d.d_rope = 16; d.d_v = 32; d.d_c = 64;",
+        "  d.dtype = KDTV_F32; d.t_stride = 64; d.scale = 0.125f;",
+        "  int st = kdtv_verify_attn(&d, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,",
+        "                            NULL, 0);",
+        '  printf("%d %zu %d %s\\n", (int)(sizeof entries / sizeof entries[0]),',
+        "         kdtv_workspace_size(&d), st, kdtv_strerror(st));",
+        "  return 0;",
+        "}",
+        ""]))
+    exe = tmp_path / "caller"
+    r = subprocess.run([cc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src),
+                        "-L", lib_dir, "-lkdtv", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    count, ws, st, name = r.stdout.split()
+    assert int(count) == len(names)
+    spec = W.small_spec("c_caller", B=1, N=16, H=4, d_nope=32, d_rope=16, d_v=32, d_c=64,
+                        dtype="f32", prefix=("fixed", 0))
+    d = kdtv.make_dims(spec, dtype="f32", t_stride=64, scale=0.125)
+    assert int(ws) == kdtv.workspace_size(d) > 0
+    assert name == "KDTV_ERR_INVALID_ARG" and kdtv.STATUS[int(st)] == name
