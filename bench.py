@@ -327,15 +327,19 @@ def main():
     import numpy as np  # noqa: F401
     import torch
     from speculative_decoding_tree_mla_gb300 import workloads as W
-    rank, ws, local = dist_init(args)
     spec = W.SPECS[args.config]
     if args.cache == "fp8":
         import dataclasses
         spec = dataclasses.replace(spec, dtype="fp8kv")
-    wl = W.make(spec)
     if args.impl == "reference":
-        run_reference(args, wl, rank, ws)
+        # host-only: no process group; ranks other than 0 exit without work
+        rank = int(os.environ.get("RANK", "0"))
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank == 0:
+            run_reference(args, W.make(spec), rank, ws)
         return
+    rank, ws, local = dist_init(args)
+    wl = W.make(spec)
 
     from speculative_decoding_tree_mla_gb300 import build, kdtv
     if rank == 0:
