@@ -209,3 +209,13 @@ def test_header_is_plain_c_and_links(L, tmp_path):
     d = kdtv.make_dims(spec, dtype="f32", t_stride=64, scale=0.125)
     assert int(ws) == kdtv.workspace_size(d) > 0
     assert name == "KDTV_ERR_INVALID_ARG" and kdtv.STATUS[int(st)] == name
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every call raises: there is no CPU fallback."""
+    monkeypatch.setattr(kdtv, "LIB_PATH", str(tmp_path / "libkdtv.so"))
+    monkeypatch.setattr(kdtv, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        kdtv.workspace_size(_dims())
+    with pytest.raises(RuntimeError, match="missing"):
+        kdtv.strerror(0)
