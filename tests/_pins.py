@@ -247,6 +247,42 @@ def pin_paged(seed=9, B=3, N=7, L=150):
     return pin_sdpa(wl)
 
 
+def pin_ragged_batch(seed=10):
+    """Requests with different prefix lengths (0, 17, 41) and shapes in which no
+    two dimensions are equal: each request equals decompressed SDPA over its
+    own rows.  Cache rows past each request's L_b + N hold NaN, so reading
+    another request's rows or past a request's end shows up as a non-finite
+    output."""
+    rng = np.random.default_rng(seed)
+    B, N, H, dn, dr, dv, dc = 3, 9, 3, 12, 6, 10, 20
+    L = np.array([0, 17, 41])
+    T = int(L.max()) + N + 5
+    parents = np.stack([W.random_tree(rng, N, None, 5) for _ in range(B)])
+    q_nope = rng.standard_normal((B, N, H, dn))
+    q_rope = rng.standard_normal((B, N, H, dr))
+    W_UK = rng.standard_normal((H, dn, dc)) / math.sqrt(dc)
+    W_UV = rng.standard_normal((H, dv, dc)) / math.sqrt(dc)
+    ckv = np.full((B, T, dc), np.nan)
+    kr = np.full((B, T, dr), np.nan)
+    for b in range(B):
+        ckv[b, :L[b] + N] = rng.standard_normal((L[b] + N, dc))
+        kr[b, :L[b] + N] = rng.standard_normal((L[b] + N, dr))
+    scale = 1 / math.sqrt(dn + dr)
+    out = oracle.verify_attn(q_nope, q_rope, W_UK, W_UV, ckv, kr, parents, L, scale)
+    if not np.all(np.isfinite(out)):
+        return float("inf")
+    err = 0.0
+    for b in range(B):
+        Lb = int(L[b])
+        mask = np.zeros((N, Lb + N), dtype=bool)
+        mask[:, :Lb] = True
+        mask[:, Lb:] = closure_mask(parents[b])
+        ref = decompressed_sdpa(q_nope[b], q_rope[b], W_UK, W_UV, ckv[b, :Lb + N],
+                                kr[b, :Lb + N], mask, scale)
+        err = max(err, float(np.abs(out[b] - ref).max()))
+    return err
+
+
 def all_pins():
     wl = tiny_inputs()
     return {
@@ -260,4 +296,5 @@ def all_pins():
         "star": lambda: pin_star(),
         "empty_prefix": lambda: pin_empty_prefix(),
         "paged": lambda: pin_paged(),
+        "ragged_batch": lambda: pin_ragged_batch(),
     }

@@ -135,9 +135,21 @@ def _m_paged_ignores_table(c_kv, k_rope, b, positions, page_table=None, page_siz
     return ORIG["gather_cache"](c_kv, k_rope, b, positions, page_table, page_size)
 
 
+def _m_first_request_prefix(q_nope, q_rope, W_UK, W_UV, c_kv, k_rope, parent, prefix_len,
+                            b, i, scale, page_table=None, page_size=0, q_lat=None):
+    same = np.full_like(np.asarray(prefix_len), np.asarray(prefix_len)[0])
+    return ORIG["verify_attn_node"](q_nope, q_rope, W_UK, W_UV, c_kv, k_rope, parent, same,
+                                    b, i, scale, page_table, page_size, q_lat)
+
+
+def _m_gather_first_request(c_kv, k_rope, b, positions, page_table=None, page_size=0):
+    return ORIG["gather_cache"](c_kv, k_rope, 0 if not page_size else b, positions,
+                                page_table, page_size)
+
+
 ORIG = {n: getattr(ORACLE_MOD, n) for n in
         ("absorb", "node_scores", "visible_positions", "ancestor_path", "softmax_rows",
-         "up_project", "gather_cache")}
+         "up_project", "gather_cache", "verify_attn_node")}
 
 MUTATIONS = {
     "absorb_uses_head0": ("absorb", _m_absorb_head0),
@@ -149,6 +161,8 @@ MUTATIONS = {
     "softmax_over_heads": ("softmax_rows", _m_softmax_heads),
     "up_project_sums_heads": ("up_project", _m_up_sum_heads),
     "paged_ignores_page_table": ("gather_cache", _m_paged_ignores_table),
+    "prefix_of_first_request_for_all": ("verify_attn_node", _m_first_request_prefix),
+    "contiguous_gather_ignores_request": ("gather_cache", _m_gather_first_request),
 }
 
 
