@@ -206,7 +206,10 @@ int kdtv_compact_kv(const kdtv_dims* dims, void* c_kv, void* k_rope,
                     const int32_t* page_table, unsigned int* status, cudaStream_t stream);
 
 /*
- * kdtv_tree_build — best-first draft tree from per-depth top-K proposals.
+ * kdtv_tree_build — best-first draft tree from per-depth top-K proposals
+ * ("The Moment of Proof: Validating a Native CUDA Speculative Decoding
+ * Engine", section "The Context: Building a Native DDTree Engine from
+ * Scratch": the GPU builder that replaces a per-request CPU heap).
  * Node 0 is the root (root_token[b], depth 0, score 0).  A node at depth d < D
  * offers K candidate children (tokens[b][d][k], score + logp[b][d][k], float32
  * addition); the best candidate (highest score, then lower parent index, then
@@ -214,6 +217,7 @@ int kdtv_compact_kv(const kdtv_dims* dims, void* c_kv, void* k_rope,
  *   logp [B, D, K] float32, tokens [B, D, K] int32, root_token [B] int32
  *   parent, token, depth [B, N] int32 out; score [B, N] float32 out (node
  *   order is topological; unused slots are -1 / -inf); n_nodes [B] int32 out.
+ * logp must hold no NaN: the place of a NaN score in the order is unspecified.
  * Returns KDTV_ERR_INVALID_ARG, KDTV_ERR_UNSUPPORTED (N > 128, K > 64) or
  * KDTV_ERR_CUDA.
  */
