@@ -219,3 +219,27 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         kdtv.workspace_size(_dims())
     with pytest.raises(RuntimeError, match="missing"):
         kdtv.strerror(0)
+
+
+@pytest.mark.parametrize("flags", [0, kdtv.KDTV_FLAG_SIMT])
+def test_size_limits_on_host(L, flags):
+    """At the largest accepted batch (B N H = 2^28 query rows) the workspace size
+    is computed without overflow; one more request is refused, and so is a
+    paged cache of more than 2^30 positions per request."""
+    spec = W.small_spec("max_rows", B=(1 << 28) // (128 * 64), N=128, H=64)
+    d = kdtv.make_dims(spec, dtype="bf16", t_stride=128, flags=flags)
+    if flags == 0 and kdtv.workspace_size(_dims(flags=0)) == 0:
+        pytest.skip("tensor-core path not compiled in")
+    rows = spec.B * spec.N * spec.H
+    assert rows == 1 << 28
+    assert kdtv.workspace_size(d) >= 2 * rows * spec.d_c * 2     # q_lat + o_lat, >= bf16 each
+    d.B += 1
+    assert kdtv.workspace_size(d) == 0
+    fake = 256
+    rc = kdtv.verify_attn_raw(d, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, 0)
+    assert kdtv.STATUS[rc] == "KDTV_ERR_UNSUPPORTED"
+    paged = kdtv.make_dims(W.SPECS["kimi_single"], dtype="bf16", page_size=64,
+                           max_pages=(1 << 24) + 1, num_pages=1 << 20, flags=flags)
+    assert kdtv.workspace_size(paged) == 0
+    rc = kdtv.verify_attn_raw(paged, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 0)
+    assert kdtv.STATUS[rc] == "KDTV_ERR_INVALID_ARG"
