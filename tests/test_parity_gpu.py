@@ -1,12 +1,17 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
-Tolerances: fp32 inputs max |err| <= 1e-5 (the pages' fp32 logit agreement
-8.106e-6, "The Moment of Truth: Validating a Custom CUDA Inference Engine for
-Kimi K2.6", opening section); bf16 inputs relative L2 <= 5e-3 and max |err|
-<= 2e-2.  The greedy token through a fixed random LM head must equal the
-oracle's wherever the oracle's top-1 margin exceeds what the relative-L2
-tolerance can move (see ``argmax_mismatches``); near-ties must still pick a
-token within that margin.
+Tolerances: fp32 arithmetic (fp32 inputs, or any input on the CUDA-core
+path) max |err| <= 1e-5 (the pages' fp32 logit agreement 8.106e-6, "The
+Moment of Truth: Validating a Custom CUDA Inference Engine for Kimi K2.6",
+opening section); the bf16 tensor-core path relative L2 <= 5e-3 and max
+|err| <= 2e-2, per node as well as over the whole output.
+
+Greedy token through a fixed random LM head (``greedy_flips``): on the fp32
+paths it must equal the oracle's on every node.  On the bf16 tensor-core
+path every flip is counted and reported, and each must sit inside the window
+that a relative-L2 error of 5e-3 in a direction unrelated to the (random,
+independent) LM head can move the top-2 logit gap: six standard deviations,
+``6 * 5e-3 * ||out|| * ||W[:,a] - W[:,b]|| / sqrt(H d_v)``.
 """
 
 import numpy as np
@@ -14,6 +19,7 @@ import pytest
 import torch
 
 import oracle
+from tests import _oracle_pool
 from speculative_decoding_tree_mla_gb300 import kdtv, workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -62,36 +68,35 @@ def all_nodes(wl):
     return [(b, i) for b in range(wl.spec.B) for i in range(wl.spec.N)]
 
 
-def sample_nodes(wl, k_req=4, seed=0):
-    rng = np.random.default_rng(seed)
-    B, N = wl.spec.B, wl.spec.N
-    reqs = sorted(set([0, B - 1] + list(rng.choice(B, size=min(B, k_req), replace=False))))
-    nodes = []
-    for b in reqs:
-        for i in sorted(set([0, N - 1, int(rng.integers(N))])):
-            nodes.append((int(b), int(i)))
-    return nodes
-
-
-def argmax_mismatches(wl, got, ref, nodes, rel_tol):
-    """(#exact, #near-tie flips, #bad flips) of the greedy token per node."""
+def lm_head(wl):
     rng = np.random.default_rng(wl.spec.seed + 77)
-    Wlm = rng.standard_normal((wl.spec.H * wl.spec.d_v, wl.spec.vocab)) / np.sqrt(
-        wl.spec.H * wl.spec.d_v)
-    exact = near = bad = 0
+    D = wl.spec.H * wl.spec.d_v
+    return rng.standard_normal((D, wl.spec.vocab)) / np.sqrt(D)
+
+
+def greedy_flips(wl, got, ref, nodes, rel_tol, kappa=6.0):
+    """Nodes whose greedy token differs from the oracle's.
+
+    Returns a list of (b, i, oracle margin, window) where the window is what
+    an error of relative L2 `rel_tol` can move the gap between the oracle's
+    token a and the chosen token g, `kappa` standard deviations out, for an
+    error direction unrelated to the random LM head:
+    kappa * rel_tol * ||out|| * ||W[:,a] - W[:,g]|| / sqrt(D).
+    """
+    Wlm = lm_head(wl)
+    D = Wlm.shape[0]
+    flips = []
     for (b, i) in nodes:
+        r = ref[(b, i)] if isinstance(ref, dict) else ref[b, i]
         tg, _ = oracle.lm_head_argmax(got[b, i], Wlm)
-        tr, lr = oracle.lm_head_argmax(ref[(b, i)], Wlm)
+        tr, lr = oracle.lm_head_argmax(r, Wlm)
         if tg == tr:
-            exact += 1
             continue
-        margin = lr[tr] - lr[tg]
-        bound = rel_tol * np.linalg.norm(ref[(b, i)]) * np.linalg.norm(Wlm[:, tr] - Wlm[:, tg])
-        if margin <= bound:
-            near += 1
-        else:
-            bad += 1
-    return exact, near, bad
+        margin = float(lr[tr] - lr[tg])
+        window = kappa * rel_tol * float(np.linalg.norm(r)) * float(
+            np.linalg.norm(Wlm[:, tr] - Wlm[:, tg])) / np.sqrt(D)
+        flips.append((b, i, margin, window))
+    return flips
 
 
 def check(wl, got, nodes, *, f32=False):
@@ -103,12 +108,14 @@ def check(wl, got, nodes, *, f32=False):
     rel = float(np.linalg.norm(g - r) / np.linalg.norm(r))
     if f32:
         assert err.max() <= F32_ABS, f"max_abs {err.max():.3e}"
-        exact, near, bad = argmax_mismatches(wl, got, ref, nodes, 1e-5)
-        assert bad == 0 and near == 0
+        assert greedy_flips(wl, got, ref, nodes, F32_ABS) == []
     else:
-        assert rel <= BF16_REL and err.max() <= BF16_ABS, f"rel {rel:.3e} max {err.max():.3e}"
-        exact, near, bad = argmax_mismatches(wl, got, ref, nodes, BF16_REL)
-        assert bad == 0, f"{bad} greedy tokens differ beyond the tolerance margin"
+        node_rel = [float(np.linalg.norm(got[b, i] - ref[(b, i)]) / np.linalg.norm(ref[(b, i)]))
+                    for b, i in nodes]
+        assert rel <= BF16_REL and max(node_rel) <= BF16_REL and err.max() <= BF16_ABS, \
+            f"rel {rel:.3e} worst node {max(node_rel):.3e} max {err.max():.3e}"
+        flips = greedy_flips(wl, got, ref, nodes, BF16_REL)
+        assert all(m <= w for _, _, m, w in flips), f"greedy flips outside the window: {flips}"
     return float(err.max()), rel
 
 
@@ -184,9 +191,7 @@ def test_tc_piece_boundaries_match_simt(chunk):
     assert st1 == st2 == 0
     rel = np.linalg.norm(a - b) / np.linalg.norm(b)
     assert rel <= BF16_REL
-    rows_bad = (np.abs(a - b).reshape(-1, a.shape[-1]).max(axis=1) >
-                0.05 * (np.abs(b).reshape(-1, b.shape[-1]).max(axis=1) + 1e-3))
-    assert int(rows_bad.sum()) == 0
+    assert per_row_rel(a, b).max() <= ROW_REL
     check(wl, a, [(bi, i) for bi in range(wl.spec.B) for i in (0, wl.spec.N // 2, wl.spec.N - 1)])
 
 
@@ -242,16 +247,97 @@ def test_tc_attention_with_simt_projections(paged):
     assert st2 == 0 and np.linalg.norm(a - b) / np.linalg.norm(b) <= BF16_REL
 
 
-# -- full-size workloads, sampled nodes -------------------------------------------
-@pytest.mark.parametrize("path", list(PATH_IDS))
-@pytest.mark.parametrize("name", ["kimi_single", "batched", "long", "paged"])
-def test_full_size_sampled(path, name):
+# -- full-size workloads, every node ----------------------------------------------------
+FULL = ["kimi_single", "batched", "long", "paged"]
+_ORACLE = {}
+
+
+def oracle_every_node(name):
+    """Oracle output [B, N, H, d_v] of every node of a full-size workload
+    (computed once per test session, in a spawn process pool)."""
+    if name not in _ORACLE:
+        _ORACLE[name] = _oracle_pool.all_nodes(name)
+    return _ORACLE[name]
+
+
+def per_node_rel(got, ref):
+    d = (got - ref).reshape(got.shape[0], got.shape[1], -1)
+    r = ref.reshape(ref.shape[0], ref.shape[1], -1)
+    return np.linalg.norm(d, axis=-1) / np.linalg.norm(r, axis=-1)
+
+
+def per_row_rel(a, b):
+    """Relative L2 of every (request, node, head) output row of a against b."""
+    d = (a - b).reshape(-1, a.shape[-1])
+    return np.linalg.norm(d, axis=-1) / np.linalg.norm(b.reshape(-1, b.shape[-1]), axis=-1)
+
+
+# One output row is one head of one node: 128 values from a 512-long latent
+# mix.  bf16 rounds q_lat, P, the piece partials and o_lat (unit roundoff
+# 2^-9 each); four independent relative errors of that size give about
+# 4e-3 per row, and a single row of ~10^6 may land a few times further out.
+ROW_REL = 2e-2
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_every_node_tc(name):
+    """The tensor-core path on the full-size workloads, every node of every
+    request against the oracle: relative L2 per node and over the output, max
+    |err|, relative L2 per output row, and the greedy token per node."""
     wl = W.make(name)
-    _skip_tc(PATH_IDS[path], wl)
-    got, st, _ = run(wl, flags=PATH_IDS[path])
+    _skip_tc(TC, wl)
+    got, st, _ = run(wl, flags=TC)
     assert st == 0
-    nodes = sample_nodes(wl)
-    check(wl, got, nodes)
+    ref = oracle_every_node(name)
+    assert np.isfinite(got).all()
+    nrel = per_node_rel(got, ref)
+    rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+    err = float(np.abs(got - ref).max())
+    rows = per_row_rel(got, ref)
+    nodes = all_nodes(wl)
+    flips = greedy_flips(wl, got, ref, nodes, BF16_REL)
+    print(f"\n{name} tc: nodes {len(nodes)} rel_l2 {rel:.3e} worst node {nrel.max():.3e} "
+          f"max_abs {err:.3e} worst row {rows.max():.3e} greedy flips {len(flips)}: "
+          + ", ".join(f"(b={b}, i={i}, margin={m:.2e}, window={w:.2e})" for b, i, m, w in flips))
+    assert rel <= BF16_REL and nrel.max() <= BF16_REL and err <= BF16_ABS
+    assert rows.max() <= ROW_REL
+    assert all(m <= w for _, _, m, w in flips)
+
+
+@pytest.mark.parametrize("name", ["tiny"] + FULL)
+def test_full_size_every_node_fp32_exact_greedy(name):
+    """The CUDA-core path (fp32 arithmetic) on every node of every workload:
+    max |err| <= 1e-5 and the greedy token equal to the oracle's on every
+    node (no window)."""
+    wl = W.make(name)
+    got, st, _ = run(wl, flags=SIMT if wl.spec.dtype != "f32" else 0)
+    assert st == 0
+    if name == "tiny":
+        nodes = all_nodes(wl)
+        r = oracle_nodes(wl, nodes)
+        ref = np.stack([np.stack([r[(b, i)] for i in range(wl.spec.N)]) for b in range(wl.spec.B)])
+    else:
+        ref = oracle_every_node(name)
+    err = float(np.abs(got - ref).max())
+    flips = greedy_flips(wl, got, ref, all_nodes(wl), F32_ABS)
+    print(f"\n{name} fp32 path: max_abs {err:.3e} rel_l2 "
+          f"{np.linalg.norm(got - ref) / np.linalg.norm(ref):.3e} greedy flips {len(flips)}")
+    assert err <= F32_ABS
+    assert flips == []
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_tc_matches_simt_per_row(name):
+    """The two CUDA paths agree on every output row of the full-size
+    workloads (a wrong 128-row tile would put whole rows far outside)."""
+    wl = W.make(name)
+    _skip_tc(TC, wl)
+    a, st1, _ = run(wl, flags=TC)
+    b, st2, _ = run(wl, flags=SIMT)
+    assert st1 == st2 == 0
+    rows = per_row_rel(a, b)
+    assert rows.max() <= ROW_REL, f"worst row {rows.max():.3e} at {int(rows.argmax())}"
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) <= BF16_REL
 
 
 # -- device-side error reporting ----------------------------------------------------
@@ -319,16 +405,3 @@ def test_device_timeout_reported_and_context_usable():
     got, st, _ = run(wl)
     assert st == 0
     check(wl, got, all_nodes(wl))
-
-
-@pytest.mark.parametrize("name", ["kimi_single", "long"])
-def test_tc_matches_simt_closely(name):
-    """The two CUDA paths agree with each other on full-size inputs (sampled
-    rows are also checked against the oracle in test_full_size_sampled)."""
-    wl = W.make(name)
-    _skip_tc(TC, wl)
-    a, st1, _ = run(wl, flags=TC)
-    b, st2, _ = run(wl, flags=SIMT)
-    assert st1 == st2 == 0
-    rel = np.linalg.norm(a - b) / np.linalg.norm(b)
-    assert rel <= BF16_REL
