@@ -19,7 +19,9 @@
  *
  * Conventions shared by every entry point:
  *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The library
- *     allocates no memory; scratch lives in the caller's workspace.
+ *     allocates no memory; scratch lives in the caller's workspace.  One
+ *     exception: kdtv_verify_attn_noalloc (end of this file) takes its scratch
+ *     from a fixed array in the library's own device image.
  *   - Calls are asynchronous on `stream` (0 = legacy default stream) and never
  *     synchronise, except kdtv_get_device_status.
  *   - Layouts are row-major with the last dimension contiguous.
@@ -27,8 +29,10 @@
  *     launch.  Conditions only the device can see (a malformed parent[], a
  *     prefix that overflows the cache, a bad page id, a wait that ran out) are
  *     recorded in the workspace status word; read it with
- *     kdtv_get_device_status.  The affected rows are left unwritten; nothing
- *     traps, and the CUDA context stays usable.
+ *     kdtv_get_device_status (kdtv_verify_attn_noalloc instead copies it to
+ *     its status_out argument; kdtv_get_device_status does not apply to it).
+ *     The affected rows are left unwritten; nothing traps, and the CUDA
+ *     context stays usable.
  *   - Calls that share a workspace must not overlap on the GPU.
  */
 #ifndef KDTV_H
@@ -240,14 +244,17 @@ int kdtv_tree_build(int B, int D, int K, int N, const float* logp, const int32_t
  * process exits.
  *   - Returns KDTV_ERR_UNSUPPORTED, before any launch, if the call needs more
  *     scratch than KDTV_NOALLOC_SCRATCH_BYTES (kdtv_workspace_size(dims) larger
- *     than the array); other errors as kdtv_verify_attn.
+ *     than the array); every other host-side error is the code
+ *     kdtv_verify_attn returns for the same dims and pointers.
  *   - status_out: device pointer to one unsigned int; when the call's kernels
  *     have finished it holds the call's device status (KDTV_OK or a device-side
  *     KDTV_ERR_* as kdtv_get_device_status would report).  Asynchronous on
  *     `stream` like every other entry point.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture on that device.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress), and again only if the
+ *     device's CUDA context has since been replaced; make that first call
+ *     before any stream capture on that device.  Concurrent first calls from
+ *     several host threads are safe.
  *   - All calls share the one array per device: calls that may overlap on the
  *     GPU (different streams or host threads) race and must be serialised by
  *     the caller.

@@ -138,6 +138,18 @@ int make_plan(const kdtv_dims* d, Plan* p) {
 
 using namespace kdtv;
 
+namespace kdtv {
+// Host-side plan check of a call: the status kdtv_verify_attn returns before
+// any launch for these dims (KDTV_OK, INVALID_ARG or UNSUPPORTED) and, when
+// OK, the workspace bytes it needs.
+int plan_status(const kdtv_dims* d, size_t* bytes) {
+  Plan p;
+  const int st = make_plan(d, &p);
+  if (bytes) *bytes = st == KDTV_OK ? p.total : 0;
+  return st;
+}
+}  // namespace kdtv
+
 extern "C" size_t kdtv_workspace_size(const kdtv_dims* d) {
   Plan p;
   if (make_plan(d, &p) != KDTV_OK) return 0;

@@ -227,6 +227,9 @@ cudaError_t launch_kv_widen(const Args& a, int sms, cudaStream_t s, bool pdl);
 bool absorb_tc_ok(const Args& a);
 bool combine_uproj_tc_ok(const Args& a);
 int tc_supported(const kdtv_dims* d);
+// Status kdtv_verify_attn returns on the host for these dims, and the
+// workspace bytes they need (0 unless KDTV_OK).
+int plan_status(const kdtv_dims* d, size_t* bytes);
 int tc_launches(const kdtv_dims* d, int splits);
 
 }  // namespace kdtv

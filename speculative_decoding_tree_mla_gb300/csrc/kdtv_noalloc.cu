@@ -17,6 +17,8 @@
 
 #include "kdtv_internal.cuh"
 
+#include <cuda.h>
+#include <mutex>
 #include <string.h>
 
 namespace {
@@ -24,23 +26,71 @@ namespace {
 // Fixed scratch: status word, q_lat, split-KV partials and o_lat of one call.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KDTV_NOALLOC_SCRATCH_BYTES];
 
+// Device address of g_noalloc_scratch, per device, tagged with the id of the
+// CUDA context it was looked up in.  If that context is destroyed and a new
+// one created (cudaDeviceReset, or the primary context released and retained
+// again), the module is loaded again and the array may move: a different
+// context id triggers a fresh lookup.
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];   // device address of g_noalloc_scratch, per device
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+ScratchSlot g_slot[kMaxDevices];
+std::mutex g_slot_mu;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// The driver's context queries, resolved through the runtime (the library
+// does not link libcuda).
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      return false;
+    get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess || q != cudaDriverEntryPointSuccess)
+      return false;
+    get_id = reinterpret_cast<CtxGetIdFn>(p);
+  }
+  CUcontext ctx = nullptr;
+  return get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // Host-side lookup of the array's device address.  In host code the symbol
 // g_noalloc_scratch is only a stand-in, not a device address; the real
-// address comes from cudaGetSymbolAddress, once per device, with that device
-// current.
+// address comes from cudaGetSymbolAddress, with the device current, the first
+// time a call runs in a given context on that device.
 int scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KDTV_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return KDTV_ERR_UNSUPPORTED;
-  if (!g_scratch_ptr[dev]) {
+  std::lock_guard<std::mutex> lock(g_slot_mu);
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) {
+    // No context is current on this host thread yet: the runtime binds the
+    // device's primary context during the lookup itself.
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p ||
+        !current_context_id(&ctx))
+      return KDTV_ERR_CUDA;
+    g_slot[dev].ptr = p;
+    g_slot[dev].ctx_id = ctx;
+  }
+  ScratchSlot& s = g_slot[dev];
+  if (!s.ptr || s.ctx_id != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KDTV_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    s.ptr = p;
+    s.ctx_id = ctx;
   }
-  *out = g_scratch_ptr[dev];
+  *out = s.ptr;
   return KDTV_OK;
 }
 
@@ -61,11 +111,12 @@ extern "C" int kdtv_verify_attn_noalloc(const kdtv_dims* dims, const void* q_nop
   memcpy(&d, dims, sizeof(d));
   d.workspace = nullptr;
   d.workspace_bytes = 0;
-  const size_t need = kdtv_workspace_size(&d);
-  if (need == 0) return KDTV_ERR_INVALID_ARG;
+  size_t need = 0;
+  int st = kdtv::plan_status(&d, &need);   // the same host-side codes as kdtv_verify_attn
+  if (st != KDTV_OK) return st;
   if (need > (size_t)KDTV_NOALLOC_SCRATCH_BYTES) return KDTV_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  int st = scratch_for_current_device(&scratch);
+  st = scratch_for_current_device(&scratch);
   if (st != KDTV_OK) return st;
   d.workspace = scratch;
   d.workspace_bytes = KDTV_NOALLOC_SCRATCH_BYTES;

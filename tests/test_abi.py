@@ -98,6 +98,10 @@ def test_bad_dims_rejected_on_host(L, field, value, code):
     fake = 256
     rc = kdtv.verify_attn_raw(d, fake, fake, fake, fake, fake, fake, fake, fake, 0, fake, 0)
     assert kdtv.STATUS[rc] == code
+    # the allocation-free entry point returns the same host-side code
+    rc2 = L.kdtv_verify_attn_noalloc(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake,
+                                     fake, None, fake, fake, None)
+    assert kdtv.STATUS[rc2] == code
 
 
 def test_null_pointers_and_workspace_rejected(L):

@@ -6,8 +6,11 @@ memory, server plugins limited to pre-registered buffers, processes that
 forbid device allocation after start-up).  For them the library offers a
 variant whose scratch is a fixed array in its own device image.  These tests
 check that variant against the regular workspace entry point, on two calls in
-a row (the array is shared and keeps the previous call's contents), and that
-a call needing more scratch than the array holds is refused.  This file is
+a row (the array is shared and keeps the previous call's contents): both run
+the same kernels on the same plan, so the outputs must be identical bit for
+bit.  They also check that a device-side error reaches the caller through
+status_out and clears on the next good call, and that a call needing more
+scratch than the array holds is refused.  This file is
 collected last so that a run stopping at the first failure has already run
 every other test; it also passes alone in a fresh process.
 """
@@ -21,10 +24,6 @@ import torch
 from speculative_decoding_tree_mla_gb300 import kdtv, workloads as W
 
 pytestmark = pytest.mark.gpu
-
-F32_ABS = 1e-5
-BF16_REL = 5e-3
-BF16_ABS = 2e-2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -52,11 +51,14 @@ def _workload(kind):
         return W.make("tiny")
     if kind == "bf16_contiguous":
         return W.make(W.small_spec("na_c", B=2, N=16, prefix=("uniform", 100, 600)))
+    if kind == "fp8_cache":
+        # the widened cache copies are the largest regions carved from the array
+        return W.make(W.small_spec("na_8", B=2, N=16, dtype="fp8kv", prefix=("uniform", 100, 600)))
     return W.make(W.small_spec("na_p", B=3, N=8, paged=True, prefix=("loguniform", 40, 700),
                                tree=("chain",)))
 
 
-@pytest.mark.parametrize("kind", ["tiny_fp32", "bf16_contiguous", "bf16_paged"])
+@pytest.mark.parametrize("kind", ["tiny_fp32", "bf16_contiguous", "bf16_paged", "fp8_cache"])
 def test_noalloc_matches_workspace_entry_point(kind):
     wl = _workload(kind)
     op = kdtv.for_workload(wl, "cuda")
@@ -73,12 +75,39 @@ def test_noalloc_matches_workspace_entry_point(kind):
         assert int(status.item()) == 0
         got = out.double().cpu().numpy()
         assert np.isfinite(got).all()
-        err = np.abs(got - ref)
-        if wl.spec.dtype == "f32":
-            assert err.max() <= F32_ABS
-        else:
-            rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-            assert rel <= BF16_REL and err.max() <= BF16_ABS
+        assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("fault", ["bad_tree", "bad_page"])
+def test_noalloc_reports_device_errors(fault):
+    """A malformed tree or an out-of-range page id, made on the host, reaches the
+    caller through status_out; the next good call reports KDTV_OK again."""
+    wl = W.make(W.small_spec("na_err", B=2, N=8, paged=True, prefix=("fixed", 100),
+                             tree=("chain",)))
+    op = kdtv.for_workload(wl, "cuda")
+    good = op().clone()
+    assert op.status() == 0
+    bad = {k: v.clone() for k, v in op.t.items()}
+    if fault == "bad_tree":
+        bad["parent"][1, 5] = 7                     # a parent after its child
+        want = "KDTV_ERR_BAD_TREE"
+    else:
+        bad["page_table"][0, 1] = wl.num_pages + 5   # a page id past the pool
+        want = "KDTV_ERR_BAD_PAGE"
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    out = torch.zeros_like(op.out)
+    saved, op.t = op.t, bad
+    rc = _noalloc(op, out, status)
+    op.t = saved
+    assert kdtv.STATUS[rc] == "KDTV_OK"
+    torch.cuda.synchronize()
+    assert kdtv.STATUS[int(status.item())] == want
+    status.fill_(12345)
+    rc = _noalloc(op, out, status)
+    assert kdtv.STATUS[rc] == "KDTV_OK"
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out, good)
 
 
 def test_noalloc_refuses_oversized_call():
