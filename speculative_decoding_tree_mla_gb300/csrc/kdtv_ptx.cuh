@@ -165,6 +165,36 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, DeviceStatus
   }
 }
 
+// mbarrier.test_wait never suspends the thread (try_wait may).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// The bounded wait of `wait`, by polling instead of sleeping: for a single
+// thread on the critical path, where the wake-up after a suspend-hint sleep
+// (a few hundred cycles) would be paid on every phase.  Same time limit,
+// abort flag and timeout report.
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, DeviceStatus* st,
+                                          uint64_t limit_ns, uint32_t site) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*reinterpret_cast<volatile unsigned int*>(&st->abort)) return false;
+      if (globaltimer() - t0 > limit_ns) {
+        record_error(st, KDTV_ERR_DEVICE_TIMEOUT, site);
+        return false;
+      }
+    }
+  }
+}
+
 // Spin (bounded by limit_ns, no error recorded, abort flag ignored) until the
 // phase with `parity` completes; used to let in-flight async data land.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {

@@ -491,8 +491,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       while (alive && have) {
         for (int j = pc.t0; j < pc.t1; ++j, ++g) {
           const int stg = g % kStages;
-          alive = wait(BAR(B_P_FULL), g & 1, st, limit, W_P_FULL);
-          if (alive) alive = wait(BAR(B_P_RX), g & 1, st, limit, W_P_RX);
+          // polled: this wait closes the loop softmax -> P.V -> softmax of every tile
+          alive = wait_spin(BAR(B_P_FULL), g & 1, st, limit, W_P_FULL);
+          if (alive) alive = wait_spin(BAR(B_P_RX), g & 1, st, limit, W_P_RX);
           // already complete (Q.K^T of tile g read this stage); orders the TMA data
           if (alive) alive = wait(BAR(B_KV_FULL + stg), (g / kStages) & 1, st, limit, W_KV_FULL);
           // the first P.V of a piece overwrites O: the previous piece must be written out
