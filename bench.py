@@ -9,10 +9,13 @@ split-KV combine, W_UV up-projection) on a seeded synthetic workload whose
 inputs are already resident in HBM; L2 is flushed (a 256 MiB write) before
 every timed call, outside the timed interval.  Prints ONE JSON line.
 
-The default workload is the Kimi-K2-shaped single request (64 heads,
-kv_lora 512, rope 64, prefix 4096, 64-node tree).  ``--impl reference`` times
-the fp64 CPU oracle on the same workload instead (bounded node sample per
-step, scaled to the whole call).
+The headline workload is the largest single-GPU one: the Kimi-K2-shaped
+long-context request (64 heads, kv_lora 512, rope 64, prefix 65536,
+128-node tree).  The other Kimi-shaped workloads (single request, batched,
+paged) are timed in the same run and reported under "workloads", each with
+its own roofline.  ``--impl reference`` times the fp64 CPU oracle on the
+headline workload instead (one sampled node per step, scaled to the whole
+call).
 """
 
 from __future__ import annotations
@@ -40,10 +43,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "kimi_single": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 9598208),
-    "long": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 932646400),
-    "batched": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 131602944),
-    "paged": ("379d9e915929eeb358497a0dc2bb687a1c4759fdfd5994807334395bdcf21242", 863827968),
+    "long": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 971177216 + 10801664),
+    "kimi_single": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 9597952 + 0),
+    "batched": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 110192128 + 12783104),
+    "paged": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 867852544 + 34444800),
 }
 
 
@@ -63,13 +66,16 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default="kimi_single")
+    ap.add_argument("--config", default="long")
+    ap.add_argument("--extra", default="kimi_single,batched,paged",
+                    help="other workloads timed in the same run ('' for none)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--path", default="tc", choices=["tc", "simt"])
     ap.add_argument("--cache", default="native", choices=["native", "fp8"],
                     help="fp8: the same workload with an FP8 E4M3 latent cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-only", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -189,7 +195,8 @@ def allmax(x, ws):
 # -- the oracle on the host (reference arm and cpu_baseline leg) ---------------
 def oracle_time(wl, seconds, max_nodes=None, seed=0):
     """Times the oracle on a bounded node sample (nodes in a random order drawn
-    from `seed`); returns (us per whole call, sample description, threads)."""
+    from `seed`); returns (us per whole call, sample description, threads,
+    seconds per node)."""
     import numpy as np
     import oracle
     f = wl.f32
@@ -209,22 +216,45 @@ def oracle_time(wl, seconds, max_nodes=None, seed=0):
     dt = time.perf_counter() - t0
     us_call = dt / done * len(nodes) * 1e6
     threads = int(os.environ.get("OPENBLAS_NUM_THREADS") or os.cpu_count() or 1)
-    return us_call, f"{done} of {len(nodes)} (request, node) pairs, random order", threads
+    return (us_call, f"{done} of {len(nodes)} (request, node) pairs in a random order, "
+            f"timed and scaled to all {len(nodes)}", threads, dt / done)
+
+
+def cpu_baseline_single_thread(args):
+    """The same oracle timing with one BLAS thread, in a child process (the
+    thread count is fixed when numpy loads)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-only", "--config", args.config,
+           "--cpu-seconds", str(args.cpu_seconds)]
+    if args.cache == "fp8":
+        cmd += ["--cache", "fp8"]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:   # the GPU numbers stand without it
+        return {"error": f"single-thread oracle timing failed: {e}"}
 
 
 def run_reference(args, wl, rank, ws):
+    """The reference arm: the oracle as it stands, on the host cores.  A step
+    is one (request, node) pair drawn at random for that step; `value` scales
+    its time to the whole call, `ms_per_step` is the measured step."""
     if rank != 0:
         return
-    per_step = []
+    per_step, step_s = [], []
+    threads = 1
     for k in range(args.warmup + args.steps):
-        us, sample, threads = oracle_time(wl, seconds=1e9, max_nodes=1, seed=k)
+        us, sample, threads, node_s = oracle_time(wl, seconds=1e9, max_nodes=1, seed=k)
         if k >= args.warmup:
             per_step.append(us)
+            step_s.append(node_s)
     v = statistics.mean(per_step)
     cfg = config_dict(wl)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1000.0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(step_s) * 1000.0,
+        "step": "one (request, node) pair of the workload; value = its time x the pairs of a call",
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": cfg,
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -320,51 +350,36 @@ def config_dict(wl):
             "paged": s.paged, "seed": s.seed, "l2": "flushed (256 MiB write) before every call"}
 
 
-def main():
-    args = parse()
-    if args.impl == "reference":
-        os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
-    import numpy as np  # noqa: F401
-    import torch
+def make_spec(name, cache):
     from speculative_decoding_tree_mla_gb300 import workloads as W
-    spec = W.SPECS[args.config]
-    if args.cache == "fp8":
+    spec = W.SPECS[name]
+    if cache == "fp8":
         import dataclasses
         spec = dataclasses.replace(spec, dtype="fp8kv")
-    if args.impl == "reference":
-        # host-only: no process group; ranks other than 0 exit without work
-        rank = int(os.environ.get("RANK", "0"))
-        ws = int(os.environ.get("WORLD_SIZE", "1"))
-        if rank == 0:
-            run_reference(args, W.make(spec), rank, ws)
-        return
-    rank, ws, local = dist_init(args)
-    wl = W.make(spec)
+    return spec
 
-    from speculative_decoding_tree_mla_gb300 import build, kdtv
-    if rank == 0:
-        build.build()
-    barrier(ws)
-    dev = torch.device("cuda", local)
-    flags = kdtv.KDTV_FLAG_SIMT if args.path == "simt" else 0
+
+def measure(wl, dev, flags, K, Wm, ws, flush, traffic_key=None, clocks=None):
+    """Device-timed calls of one workload with inputs resident in HBM: K calls
+    each bracketed by events on the call's stream (L2 flushed before each,
+    outside the events), then a pass with the library's phase events for the
+    attention kernel's own duration, then K back-to-back calls without the
+    flush.  Returns the workload's numbers and the op."""
+    import torch
+    from speculative_decoding_tree_mla_gb300 import kdtv
     op = kdtv.for_workload(wl, dev, flags=flags)
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    K, Wm = args.steps, max(3, args.warmup)
-
     for _ in range(Wm):
         flush.zero_()
         op()
     torch.cuda.synchronize()
     if op.status() != 0:
-        raise SystemExit(f"device status {kdtv.STATUS[op.status()]}")
+        raise SystemExit(f"{wl.spec.name}: device status {kdtv.STATUS[op.status()]}")
 
-    # Timed region: K calls, each bracketed by events on the call's stream (the
-    # library's own phase events stay off here: they would split the call).
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
-    clocks = Clocks(local)
-    clocks.start()
+    if clocks:
+        clocks.start()
     barrier(ws)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
@@ -376,15 +391,14 @@ def main():
     torch.cuda.synchronize()
     barrier(ws)
     t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else None
     st = op.status()
     if st != 0:
-        raise SystemExit(f"device status {kdtv.STATUS[st]}")
+        raise SystemExit(f"{wl.spec.name}: device status {kdtv.STATUS[st]}")
     call_ms = [a.elapsed_time(b) for a, b in ev]
 
-    # Phase pass: the library records events between its kernels (absorb,
-    # attention, split combine, up-projection); gives the attention kernel's
-    # own duration for the roofline.
+    # Phase pass: events recorded by the library between its kernels give the
+    # attention kernel's own duration (the roofline's denominator).
     K_ph = min(K, 200)
     pev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K_ph)]
     for k in range(K_ph):
@@ -393,10 +407,9 @@ def main():
         op()
     torch.cuda.synchronize()
     op.set_phase_events(None)
-    ev_phase = pev
+    phase_ms = [[e[j].elapsed_time(e[j + 1]) for e in pev] for j in range(4)]
 
-    # Warm L2: the same call back to back with no flush between calls (the
-    # headline above flushes L2 before every call).
+    # Warm L2: the same call back to back with no flush between calls.
     K_w = min(K, 500)
     wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K_w)]
@@ -405,24 +418,52 @@ def main():
         op()
         wev[k][1].record(stream)
     torch.cuda.synchronize()
-    warm_us = allmax(statistics.mean(a.elapsed_time(b) for a, b in wev), ws) * 1000.0 / ws
-    phase_ms = [[e[j].elapsed_time(e[j + 1]) for e in ev_phase] for j in range(4)]
+
     mean_ms = allmax(statistics.mean(call_ms), ws)
-    us_call = mean_ms * 1000.0 / ws        # whole job: ws replicas in parallel
     wk = work(wl)
     pk, pk_kind = peaks()
     attn_ms = statistics.mean(phase_ms[1])
     tflops = wk["attn_flops"] / (attn_ms * 1e-3) / 1e12
     peak_tc = pk["bf16_tflops"]
+    us_replica = mean_ms * 1000.0
     roof_us = max(wk["cache_bytes"] / (pk["hbm_gbs"] * 1e9),
                   wk["total_flops"] / (peak_tc * 1e12)) * 1e6
-    phases = {n: statistics.mean(x) * 1000.0 for n, x in
-              zip(["absorb_us", "attention_us", "combine_us", "up_proj_us"], phase_ms)}
+    res = {
+        "us_per_call_per_replica": us_replica,
+        "us_call": us_replica / ws,       # whole job: ws replicas run side by side
+        "mean_ms": mean_ms,
+        "p50_us": statistics.median(call_ms) * 1000.0,
+        "warm_l2_us": allmax(statistics.mean(a.elapsed_time(b) for a, b in wev), ws) * 1000.0,
+        "phases": {n: statistics.mean(x) * 1000.0 for n, x in
+                   zip(["absorb_us", "attention_us", "combine_us", "up_proj_us"], phase_ms)},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tc, "unit": "TFLOP/s",
+                     "frac": tflops / peak_tc,
+                     "traffic": attn_traffic(traffic_key) if traffic_key else None,
+                     "kernel": "attention (tree-masked scores, online softmax, P.c_kv)",
+                     "attention_us": attn_ms * 1000.0,
+                     "algorithmic_flops": wk["attn_flops"],
+                     "peak_source": f"{pk_kind} bf16_tflops (burst)"},
+        "call_roofline": {"t_roof_us": roof_us, "frac": roof_us / us_replica,
+                          "tflops": wk["total_flops"] / (us_replica * 1e-6) / 1e12,
+                          "cache_tbs": wk["cache_bytes"] / (us_replica * 1e-6) / 1e12,
+                          "flops": wk["total_flops"], "cache_bytes": wk["cache_bytes"],
+                          "all_bytes": wk["all_bytes"]},
+        "steps": K,
+        "wall_s_timed_region": t_wall,
+        "clocks": clk,
+    }
+    return res, op
 
-    # End to end: pinned host inputs -> device, call, result -> host.
-    # Every input of the call lives in one pinned host block, mirrored by one
-    # device block with the same 256-byte aligned layout (the kernels read
-    # views of it), so a step moves its inputs with a single DMA.
+
+def e2e_time(wl, op, dev, K, Wm, ws, flush):
+    """End to end through the public call: every step copies the call's inputs
+    from pinned host memory and reads the output back, inside the events.
+
+    Every input of the call lives in one pinned host block, mirrored by one
+    device block with the same 256-byte aligned layout (the kernels read views
+    of it), so a step moves its inputs with a single DMA."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
     names = ["q_nope", "q_rope", "W_UK", "W_UV", "c_kv", "k_rope", "parent", "prefix_len"]
     if wl.page_size:
         names.append("page_table")
@@ -434,17 +475,15 @@ def main():
         total += src[n].numel() * src[n].element_size()
     host_blk = torch.empty(total, dtype=torch.uint8).pin_memory()
     dev_blk = torch.empty(total, dtype=torch.uint8, device=dev)
+    saved = dict(op.t)
     for n in names:
         nb = src[n].numel() * src[n].element_size()
         host_blk[offs[n]:offs[n] + nb].copy_(src[n].view(-1).view(torch.uint8))
         op.t[n] = dev_blk[offs[n]:offs[n] + nb].view(src[n].dtype).view(src[n].shape)
-    h2d = total
     out_before = op.out.clone()
     out_host = torch.empty(op.out.shape, dtype=op.out.dtype).pin_memory()
-    d2h = out_host.numel() * out_host.element_size()
     e2e_ms = []
-    K_e2e = min(K, 200)
-    for k in range(Wm + K_e2e):
+    for k in range(Wm + K):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -456,45 +495,94 @@ def main():
         e1.synchronize()
         if k >= Wm:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_us = allmax(statistics.mean(e2e_ms), ws) * 1000.0 / ws
     # the block-backed calls compute the same output as the resident inputs did
     assert op.status() == 0 and torch.equal(op.out, out_before)
+    op.t.update(saved)
+    us = allmax(statistics.mean(e2e_ms), ws) * 1000.0 / ws
+    return {"value": us, "unit": UNIT, "h2d_bytes_per_step": total,
+            "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
 
-    steps_us = loop_steps(wl, dev) if rank == 0 else None
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+    import numpy as np  # noqa: F401
+    from speculative_decoding_tree_mla_gb300 import workloads as W
+    spec = make_spec(args.config, args.cache)
+    if args.cpu_only:
+        v, sample, threads, _ = oracle_time(W.make(spec), args.cpu_seconds)
+        print(json.dumps({"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                          "sample": sample}), flush=True)
+        return
+    if args.impl == "reference":
+        # host-only: no process group; ranks other than 0 exit without work
+        rank = int(os.environ.get("RANK", "0"))
+        ws = int(os.environ.get("WORLD_SIZE", "1"))
+        if rank == 0:
+            run_reference(args, W.make(spec), rank, ws)
+        return
+    import torch
+    rank, ws, local = dist_init(args)
+    wl = W.make(spec)
+
+    from speculative_decoding_tree_mla_gb300 import build, kdtv
+    if rank == 0:
+        build.build()
+    barrier(ws)
+    dev = torch.device("cuda", local)
+    flags = kdtv.KDTV_FLAG_SIMT if args.path == "simt" else 0
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    K, Wm = args.steps, max(3, args.warmup)
+    native = not flags and args.cache == "native"
+
+    head, op = measure(wl, dev, flags, K, Wm, ws, flush,
+                       traffic_key=args.config if native else None, clocks=Clocks(local))
+    e2e = e2e_time(wl, op, dev, min(K, 200), Wm, ws, flush)
+    launches = op.launches()
+    del op
+
+    extras = {}
+    for name in [x for x in args.extra.split(",") if x and x != args.config]:
+        wlx = W.make(make_spec(name, args.cache))
+        r, opx = measure(wlx, dev, flags, min(K, 300), Wm, ws, flush,
+                         traffic_key=name if native else None)
+        r.pop("clocks", None)
+        r["config"] = config_dict(wlx)
+        extras[name] = r
+        del opx, wlx
+        torch.cuda.empty_cache()
+
+    steps_us = loop_steps(W.make(make_spec("kimi_single", "native")), dev) if rank == 0 else None
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        v, sample, threads = oracle_time(wl, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample}
+        v, sample, threads, _ = oracle_time(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+               "single_thread": cpu_baseline_single_thread(args)}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": ws, "steps": K,
-            "warmup": Wm, "ms_per_step": mean_ms, "higher_is_better": False,
+            "metric": METRIC, "value": head["us_call"], "unit": UNIT, "n_gpus": ws, "steps": K,
+            "warmup": Wm, "ms_per_step": head["mean_ms"], "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32" if (op.dims.dtype == kdtv.KDTV_F32 or flags) else "bf16",
+            "dtype": "f32" if (wl.spec.dtype == "f32" or flags) else "bf16",
             "data": "synthetic", "config": config_dict(wl),
-            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_tc,
-                         "unit": "TFLOP/s", "frac": tflops / peak_tc,
-                         "traffic": (attn_traffic(args.config)
-                                     if not flags and args.cache == "native" else None),
-                         "kernel": "attention (tree-masked scores, online softmax, P.c_kv)",
-                         "peak_source": f"{pk_kind} bf16_tflops (burst)"},
-            "call_roofline": {"t_roof_us": roof_us, "frac": roof_us / us_call,
-                              "tflops": wk["total_flops"] / (us_call * 1e-6) / 1e12,
-                              "cache_tbs": wk["cache_bytes"] / (us_call * 1e-6) / 1e12,
-                              "flops": wk["total_flops"], "cache_bytes": wk["cache_bytes"],
-                              "all_bytes": wk["all_bytes"]},
-            "phases": phases,
-            "loop_steps": steps_us,
-            "p50_us": statistics.median(call_ms) * 1000.0,
-            "warm_l2_us": warm_us,
-            "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "gpu_launches": op.launches() * K,
+            "roofline": head["roofline"],
+            "call_roofline": head["call_roofline"],
+            "phases": head["phases"],
+            "p50_us": head["p50_us"],
+            "warm_l2_us": head["warm_l2_us"],
+            "us_per_call_per_replica": head["us_per_call_per_replica"],
+            "value_note": ("value = mean device time of one call on one GPU divided by the "
+                           "number of GPUs (each GPU runs its own replica of the call)"),
+            "e2e": e2e,
+            "gpu_launches": launches * K,
             "path": args.path,
-            "clocks": clk,
-            "wall_s_timed_region": t_wall,
+            "clocks": head["clocks"],
+            "wall_s_timed_region": head["wall_s_timed_region"],
+            "workloads": extras,
+            "loop_steps": steps_us,
         }
         if cpu:
             line["cpu_baseline"] = cpu
