@@ -43,10 +43,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "long": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 971177216 + 10801664),
-    "kimi_single": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 9597952 + 0),
-    "batched": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 110192128 + 12783104),
-    "paged": ("bbe54ca4bd1185849228db2d6102040b905a166ed635b9c9c47fe04213891e08", 867852544 + 34444800),
+    "long": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 929099008 + 10783488),
+    "kimi_single": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 9601024 + 0),
+    "batched": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 109074432 + 12553216),
+    "paged": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 941420544 + 35295232),
 }
 
 

@@ -37,12 +37,21 @@
 //
 // TMEM (512 columns per CTA): O_c [0, 256) fp32; q_lat half [256, 384) as
 // bf16 pairs (the A operand of Q.K^T); two score buffers [384, 448) and
-// [448, 512).  Shared memory: a 4-stage TMA ring of 64-key cache tiles
-// (128-byte swizzled 64-column chunks; the same tile is the K-major B operand
-// of Q.K^T and the MN-major B operand of P.V), q_rope (CTA 0), the P tile
-// (K-major A operand of P.V), two receive buffers for the peer's scores and
-// four for its rescale factors.  Key tiles are also prefetched into L2 a few
-// tiles ahead of the ring.
+// [448, 512).  Shared memory (all of the 227 KiB a CTA may have; the dynamic
+// base must be 1 KiB aligned, which the kernel checks):
+//   - a 5-slot TMA ring of the latent half of 64-key cache tiles (128-byte
+//     swizzled 64-column chunks; the same slot is the K-major B operand of
+//     Q.K^T and the MN-major B operand of P.V), freed by P.V;
+//   - a 2-slot ring of the tiles' rope halves, freed as soon as Q.K^T read
+//     them (the rope only enters Q.K^T);
+//   - q_rope (this CTA's 32 rope dimensions of the piece's rows);
+//   - TWO P tiles (K-major A operand of P.V), for even and odd key tiles, so
+//     that the softmax of tile g writes P while P.V of tile g-1 still reads the
+//     other one: only a rescale of O (rare with the lazy reference maxima)
+//     waits for P.V of tile g-1;
+//   - two receive buffers for the peer's scores, four for its rescale factors
+//     and the reference maxima and row sums of the 64 rows each CTA owns.
+// Key tiles are also prefetched into L2 a few tiles ahead of the ring.
 //
 // Warp roles (480 threads): warp 0 issues TMA loads; warp 1 owns TMEM and
 // issues Q.K^T; warps 2-5 (one per lane quadrant) load each piece's Q into
@@ -72,12 +81,13 @@ constexpr int BM = 128;          // query rows per tile (MMA M)
 constexpr int BN = 64;           // keys per tile (MMA N of Q.K^T)
 constexpr int CH = 64;           // bf16 columns per 128-byte swizzled chunk
 constexpr int kHalf = 256;       // latent columns per CTA
-constexpr int kStages = 5;
+constexpr int kStages = 5;       // latent ring slots (freed by P.V)
+constexpr int kRopeSlots = 2;    // rope ring slots (freed by Q.K^T)
 constexpr int kPrefetch = 3;     // key tiles prefetched into L2 beyond the stages in flight
 constexpr int kRopeHalf = 32;    // rope dimensions per CTA (64-byte rows, 64-byte swizzle)
 constexpr int kKVChunk = BN * CH * 2;   // 8 KiB
 constexpr int kRopeChunk = BN * kRopeHalf * 2;            // 4 KiB of k_rope per key tile
-constexpr int kStageBytes = 4 * kKVChunk + kRopeChunk;    // 4 latent chunks + the rope half
+constexpr int kStageBytes = 4 * kKVChunk;                 // 4 latent chunks of 64 columns
 constexpr int kQRopeBytes = BM * kRopeHalf * 2;
 constexpr int kPBytes = BM * BN * 2;    // the P tile: 128 rows x 64 keys bf16, 128B-swizzled
 constexpr int kPQuadBytes = 16 * BN * 2;   // one quadrant's own P rows (contiguous, 2 KiB)
@@ -86,7 +96,7 @@ constexpr int kPQuadBytes = 16 * BN * 2;   // one quadrant's own P rows (contigu
 // ((q * 4 + m) * 32 + t) * 16, so one warp store is a contiguous 512-byte
 // block; then one word per (q, t) holding its two rows' shifts.
 constexpr int kRxData = 4 * 4 * 32 * 16;
-constexpr int kRxBytes = kRxData + 4 * 32 * 4;
+constexpr int kRxBytes = kRxData + 4 * 8 * 4;   // + one shift word per row pair
 constexpr int kRxStride = (kRxBytes + 127) / 128 * 128;
 constexpr int kAfBufs = 4;              // rescale-factor buffers, [BM] floats each
 constexpr int kAfBytes = 64 * 4;        // the peer's 64 rows per tile
@@ -98,18 +108,20 @@ constexpr int kColQ = 256;
 constexpr int kColS = 384;       // + 64 * buffer
 
 constexpr int OFF_KV = 0;
-constexpr int OFF_QR = OFF_KV + kStages * kStageBytes;
-constexpr int OFF_P = OFF_QR + kQRopeBytes;
-constexpr int OFF_RX = OFF_P + kPBytes;                        // two receive buffers
-constexpr int OFF_AF = OFF_RX + 2 * kRxStride;                 // [kAfBufs][BM] floats
-constexpr int OFF_MREF = OFF_AF + kAfBufs * BM * 4;             // [2 parities][BM] reference maxima
-constexpr int OFF_LPART = OFF_MREF + 2 * BM * 4;                // [m | l][BM] of the odd-tile warps
-constexpr int OFF_BAR = OFF_LPART + 2 * BM * 4;
-constexpr int kNumBars = 48;
+constexpr int OFF_ROPE = OFF_KV + kStages * kStageBytes;       // [kRopeSlots] rope halves
+constexpr int OFF_QR = OFF_ROPE + kRopeSlots * kRopeChunk;
+constexpr int OFF_P = OFF_QR + kQRopeBytes;                    // two P tiles (even / odd key tiles)
+constexpr int OFF_RX = OFF_P + 2 * kPBytes;                    // two receive buffers
+constexpr int OFF_AF = OFF_RX + 2 * kRxStride;                 // [kAfBufs][64] floats (peer rows)
+constexpr int OFF_MREF = OFF_AF + kAfBufs * 64 * 4;             // [2 parities][64] reference maxima
+constexpr int OFF_LPART = OFF_MREF + 2 * 64 * 4;                // [m | l][64] of the odd-tile warps
+constexpr int OFF_BAR = OFF_LPART + 2 * 64 * 4;
+constexpr int kNumBars = 50;
 constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
-constexpr int kSmemBytes = OFF_MISC + 64 + 1024;   // + slack for 1 KiB alignment
+constexpr int kSmemBytes = OFF_MISC + 64;   // the base must be 1 KiB aligned (checked)
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(kStageBytes % 1024 == 0 && OFF_QR % 1024 == 0 && OFF_P % 1024 == 0,
+static_assert(kStageBytes % 1024 == 0 && OFF_ROPE % 1024 == 0 && kRopeChunk % 1024 == 0 &&
+              OFF_QR % 1024 == 0 && OFF_P % 1024 == 0 && kPBytes % 1024 == 0,
               "swizzled tiles need 1 KiB alignment");
 static_assert(OFF_RX % 16 == 0 && kRxStride % 16 == 0 && OFF_AF % 16 == 0, "async store alignment");
 static_assert(kThreads == 32 * (kWarpPV + 1), "warp roles");
@@ -118,16 +130,17 @@ static_assert(kThreads == 32 * (kWarpPV + 1), "warp roles");
 enum Bar : int {
   B_QR_FULL = 0,
   B_Q_READY = 1,                     // 8 warps stored their part of Q in TMEM
-  B_KV_FULL = 2,                     // [kStages]
-  B_KV_EMPTY = B_KV_FULL + kStages,  // [kStages]
-  B_S_FULL = B_KV_EMPTY + kStages,   // [2] Q.K^T of the tile completed
+  B_KV_FULL = 2,                     // [kStages] latent slot and its tile's rope slot landed
+  B_KV_EMPTY = B_KV_FULL + kStages,  // [kStages] P.V read the latent slot
+  B_R_EMPTY = B_KV_EMPTY + kStages,  // [kRopeSlots] Q.K^T read the rope slot
+  B_S_FULL = B_R_EMPTY + kRopeSlots, // [2] Q.K^T of the tile completed
   B_S_FREE = B_S_FULL + 2,           // [2] senders and softmax read the scores
-  B_RX_FULL = B_S_FREE + 2,          // [2] the peer's score rows landed (tx)
-  B_TX_OK = B_RX_FULL + 2,           // [2] the peer consumed what we sent (remote)
+  B_RX_FULL = B_S_FREE + 2,          // [2] the peer's score rows landed in receive buffer g & 1 (tx)
+  B_TX_OK = B_RX_FULL + 2,           // [2] the peer consumed what we sent into buffer g & 1 (remote)
   B_AF_FULL = B_TX_OK + 2,           // [kAfBufs] the peer's rescale factors landed (tx)
-  B_P_FULL = B_AF_FULL + kAfBufs,    // our softmax wrote its P rows
-  B_P_RX = B_P_FULL + 1,             // the peer's P rows landed (tx)
-  B_P_EMPTY = B_P_RX + 1,            // [2] P.V of an even / odd tile completed in both CTAs
+  B_P_FULL = B_AF_FULL + kAfBufs,    // [2] our softmax wrote its P rows of an even / odd tile
+  B_P_RX = B_P_FULL + 2,             // [2] the peer's P rows of an even / odd tile landed (tx)
+  B_P_EMPTY = B_P_RX + 2,            // [2] P.V of an even / odd tile completed in both CTAs
   B_O_FULL = B_P_EMPTY + 2,          // [2] a piece's O is complete, for the even / odd-tile warps
   B_MMA_DONE = B_O_FULL + 2,         // both MMA issuers drained
   B_STALL = B_MMA_DONE + 1,
@@ -211,6 +224,10 @@ __device__ bool piece_next(const Args& a, int end, int W, Piece& p) {
 // Keeps a value computed before the next wait: the compiler may otherwise
 // sink arithmetic whose result is only used after a wait below it, onto the
 // critical path that the wait ends.
+// Compact index of a softmax row among a CTA's 64 own (or the peer's 64) rows:
+// rows 32q + 16 rank + i of quadrant q map to 16q + i.
+__device__ __forceinline__ int crow(int r) { return 16 * (r >> 5) + (r & 15); }
+
 __device__ __forceinline__ void pin(uint32_t& x) { asm volatile("" : "+r"(x)); }
 __device__ __forceinline__ void pin(float& x) { asm volatile("" : "+f"(x)); }
 
@@ -304,11 +321,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                const __grid_constant__ CUtensorMap tm_ckv,
                const __grid_constant__ CUtensorMap tm_krope, const Args a, const TcCfg cfg) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   const uint32_t sbase = smem_u32(sm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (sbase & 1023u) {   // swizzled tiles need a 1 KiB aligned base (no slack is reserved)
+    if (tid == 0) record_error(a.status, KDTV_ERR_UNSUPPORTED, 0xA11u);
+    return;
+  }
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int cl = blockIdx.x >> 1;                  // this CTA pair
@@ -326,15 +346,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       mbar_init(BAR(B_KV_FULL + i), 1);
       mbar_init(BAR(B_KV_EMPTY + i), 1);
     }
+    for (int i = 0; i < kRopeSlots; ++i) mbar_init(BAR(B_R_EMPTY + i), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(B_S_FULL + i), 1);
       mbar_init(BAR(B_S_FREE + i), 8);    // 4 sender + 4 softmax warps read the scores
+      mbar_init(BAR(B_P_FULL + i), 4);    // the tile's 4 softmax warps
+      mbar_init(BAR(B_P_RX + i), 1);      // armed with expect_tx; filled by the peer's bulk copies
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(BAR(B_RX_FULL + i), 1);   // armed with expect_tx; filled by the peer's st.async
-      mbar_init(BAR(B_TX_OK + i), 4);     // one relaxed arrival per peer softmax warp
+      mbar_init(BAR(B_TX_OK + i), 4);     // one arrival per peer softmax warp of the tile
     }
     for (int i = 0; i < kAfBufs; ++i) mbar_init(BAR(B_AF_FULL + i), 1);
-    mbar_init(BAR(B_P_FULL), 4);          // the tile's 4 softmax warps
-    mbar_init(BAR(B_P_RX), 1);            // armed with expect_tx; filled by the peer's bulk copies
     // P.V commits of both CTAs (multicast), one barrier per tile parity: each
     // softmax warp waits only for the other parity's tiles, so it sees every
     // phase of the barrier it waits on in order.
@@ -350,10 +373,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     mbar_init(BAR(B_QR_EMPTY), 1);
     mbar_init(BAR(B_O_FREE), 4);          // the 4 softmax warps that wrote a piece's O out
     mbar_init(BAR(B_L_FREE), 4);          // the even-tile warps read the hand-over
-    mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // exchanges of tiles 0 and 1
+    mbar_expect_tx(BAR(B_RX_FULL + 0), kRxBytes);   // the score exchanges of tiles 0 and 1
     mbar_expect_tx(BAR(B_RX_FULL + 1), kRxBytes);
     for (int i = 0; i < kAfBufs; ++i) mbar_expect_tx(BAR(B_AF_FULL + i), kAfBytes);
-    mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes);
+    mbar_expect_tx(BAR(B_P_RX + 0), 4 * kPQuadBytes);   // the peer's P rows of tiles 0 and 1
+    mbar_expect_tx(BAR(B_P_RX + 1), 4 * kPQuadBytes);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -411,19 +435,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         for (int j = pc.t0 + kStages; j < pc.t0 + kStages + kPrefetch && j < pc.t1; ++j)
           prefetch(pc.b, j * BN);
         for (int j = pc.t0; j < pc.t1; ++j, ++g) {
-          const int stg = g % kStages;
+          const int stg = g % kStages, rs = g % kRopeSlots;
           if (g >= kStages &&
               !wait(BAR(B_KV_EMPTY + stg), ((g / kStages) - 1) & 1, st, limit, W_KV_EMPTY)) {
             alive = false;
             break;
           }
+          if (g >= kRopeSlots &&
+              !wait(BAR(B_R_EMPTY + rs), ((g / kRopeSlots) - 1) & 1, st, limit, W_KV_EMPTY)) {
+            alive = false;
+            break;
+          }
           const int row = key_row(pc.b, j * BN);
-          mbar_expect_tx(BAR(B_KV_FULL + stg), kStageBytes);
+          mbar_expect_tx(BAR(B_KV_FULL + stg), kStageBytes + kRopeChunk);
           const uint32_t dst = sbase + OFF_KV + stg * kStageBytes;
           for (int c = 0; c < 4; ++c)
             tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
                         (int)rank * kHalf + c * CH, row);
-          tma_load_2d(dst + 4 * kKVChunk, &tm_krope, BAR(B_KV_FULL + stg), kRopeHalf * (int)rank, row);
+          tma_load_2d(sbase + OFF_ROPE + rs * kRopeChunk, &tm_krope, BAR(B_KV_FULL + stg),
+                      kRopeHalf * (int)rank, row);
           issued = g + 1;
           if (j + kStages + kPrefetch < pc.t1) prefetch(pc.b, (j + kStages + kPrefetch) * BN);
         }
@@ -462,13 +492,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
             uint64_t bd = smem_desc(kv + (kk >> 2) * kKVChunk + (kk & 3) * 32, 16, 1024);
             mma_bf16_ts(d, tmem + kColQ + 8 * kk, bd, kIdescQK, kk > 0);
           }
+          const uint32_t kr = sbase + OFF_ROPE + (g % kRopeSlots) * kRopeChunk;
 #pragma unroll
           for (int kk = 0; kk < kRopeHalf / 16; ++kk) {   // rope half: A = q_rope half in smem
             uint64_t ad = smem_desc_sw64(sbase + OFF_QR + kk * 32, 16, 512);
-            uint64_t bd = smem_desc_sw64(kv + 4 * kKVChunk + kk * 32, 16, 512);
+            uint64_t bd = smem_desc_sw64(kr + kk * 32, 16, 512);
             mma_bf16(d, ad, bd, kIdescQK, 1);
           }
           mma_commit(BAR(B_S_FULL + buf));
+          mma_commit(BAR(B_R_EMPTY + g % kRopeSlots));   // the rope slot may be refilled
         }
         if (!alive) break;
         mma_commit(BAR(B_Q_EMPTY));                 // Q (and q_rope) may be reloaded
@@ -486,29 +518,36 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
       Piece pc;
       bool have = piece_first(a, cl, beg, end, W, pc);
-      int g = 0, pi = 0, p_armed = 1;              // phases of B_P_RX armed so far
+      int g = 0, pi = 0;
+      // phases of B_P_RX + b armed and consumed so far (both armed at set-up)
+      int p_armed0 = 1, p_armed1 = G > 1 ? 1 : 0, p_used0 = 0, p_used1 = 0;
       bool alive = true;
       while (alive && have) {
         for (int j = pc.t0; j < pc.t1; ++j, ++g) {
-          const int stg = g % kStages;
-          // polled: this wait closes the loop softmax -> P.V -> softmax of every tile
-          alive = wait_spin(BAR(B_P_FULL), g & 1, st, limit, W_P_FULL);
-          if (alive) alive = wait_spin(BAR(B_P_RX), g & 1, st, limit, W_P_RX);
+          const int stg = g % kStages, pb = g & 1;
+          alive = wait_spin(BAR(B_P_FULL + pb), (g >> 1) & 1, st, limit, W_P_FULL);
+          if (alive) alive = wait_spin(BAR(B_P_RX + pb), (g >> 1) & 1, st, limit, W_P_RX);
+          if (alive) (pb ? p_used1 : p_used0) += 1;
           // already complete (Q.K^T of tile g read this stage); orders the TMA data
           if (alive) alive = wait(BAR(B_KV_FULL + stg), (g / kStages) & 1, st, limit, W_KV_FULL);
           // the first P.V of a piece overwrites O: the previous piece must be written out
           if (alive && j == pc.t0 && pi >= 1)
             alive = wait(BAR(B_O_FREE), (pi - 1) & 1, st, limit, W_O_FREE);
           if (!alive) break;
-          // arm the peer's P rows of tile g+1 before our commit lets the peer send them
-          if (g + 1 < G) { mbar_expect_tx(BAR(B_P_RX), 4 * kPQuadBytes); ++p_armed; }
+          // arm the peer's P rows of tile g+2 (same buffer) before our commit lets the
+          // peer send them
+          if (g + 2 < G) {
+            mbar_expect_tx(BAR(B_P_RX + pb), 4 * kPQuadBytes);
+            (pb ? p_armed1 : p_armed0) += 1;
+          }
           tc_fence_after();
           const uint32_t kv = sbase + OFF_KV + stg * kStageBytes;
+          const uint32_t pt = sbase + OFF_P + pb * kPBytes;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             // A = P (K-major, 128B rows); B = V = c_kv columns of this CTA,
             // MN-major: 64-column chunks kKVChunk apart (LBO), 8-key groups 1 KiB apart (SBO).
-            uint64_t ad = smem_desc(sbase + OFF_P + kk * 32, 16, 1024);
+            uint64_t ad = smem_desc(pt + kk * 32, 16, 1024);
             uint64_t bd = smem_desc(kv + kk * 16 * 128, kKVChunk, 1024);
             mma_bf16(tmem + kColO, ad, bd, kIdescPV, (j > pc.t0 || kk > 0));
           }
@@ -524,7 +563,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         ++pi;
       }
       // After an abort: let the peer's P rows of an armed, unconsumed phase land.
-      if (!alive && p_armed > 0) drain_wait(BAR(B_P_RX), (p_armed - 1) & 1, 200000ull);
+      if (!alive) {
+        if (p_armed0 > p_used0) drain_wait(BAR(B_P_RX + 0), (p_armed0 - 1) & 1, 200000ull);
+        if (p_armed1 > p_used1) drain_wait(BAR(B_P_RX + 1), (p_armed1 - 1) & 1, 200000ull);
+      }
       mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
       wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
     }
@@ -626,8 +668,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           for (int m = 0; m < 4; ++m)
             st_async_v4u(rxp + ((q * 4 + m) * 32 + lane) * 16, w[4 * m], w[4 * m + 1], w[4 * m + 2],
                          w[4 * m + 3], rxfull_remote);
-          st_async_u32(rxp + kRxData + (q * 32 + lane) * 4,
-                       ((uint32_t)sha & 0xffffu) | ((uint32_t)shb << 16), rxfull_remote);
+          if (c == 0)   // the row pair's four threads hold the same shifts
+            st_async_u32(rxp + kRxData + (q * 8 + (lane >> 2)) * 4,
+                         ((uint32_t)sha & 0xffffu) | ((uint32_t)shb << 16), rxfull_remote);
         }
         ++pi;
         have = piece_next(a, end, W, pc);
@@ -649,7 +692,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
       // running reference maxima pass between the two warps of the quadrant
       // through shared memory (restarting at -inf with every piece).
       int g = 0, pi = 0;
-      int next_rx = par;                          // first receive phase not yet consumed
+      int next_rx = par;                          // first tile whose scores this warp has not received
       int next_af = par;
       // Writes O columns [col0, col0 + 32 nch32) of rows 32q .. 32q+31 of a piece
       // (row tile rt, partial slot `slot`) once its P.V completed, then frees O.
@@ -686,7 +729,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(B_S_FREE + buf));   // QK^T of tile g+2 may overwrite
 
-          // + the peer's partial scores for our rows (its st.async filled rx[buf])
+          // + the peer's partial scores for our rows (its st.async filled rx[buf]);
+          // the lead warp arms this buffer for tile g+2
           alive = __all_sync(0xffffffffu,
                              wait<true>(BAR(B_RX_FULL + buf), (g >> 1) & 1, st, limit, W_RX_FULL));
           if (!alive) break;
@@ -701,7 +745,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
               asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(pw[4 * m]), "=r"(pw[4 * m + 1]), "=r"(pw[4 * m + 2]), "=r"(pw[4 * m + 3])
                            : "r"(rxb + ((q * 4 + m) * 32 + lane) * 16) : "memory");
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(shw) : "r"(rxb + kRxData + (q * 32 + lane) * 4)
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(shw) : "r"(rxb + kRxData + (q * 8 + (lane >> 2)) * 4)
                          : "memory");
             const float pia = pow2f(-(int)(int16_t)(shw & 0xffffu));
             const float pib = pow2f(-(int)(int16_t)(shw >> 16));
@@ -716,7 +760,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
             }
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));  // consumed
+          // consumed: the peer may overwrite the buffer (release: after our reads)
+          if (lane == 0) mbar_arrive_remote_relaxed(mapa(BAR(B_TX_OK + buf), peer));
 
           // visibility mask (only tiles that reach past the prefix, or rows past the end);
           // each row's ancestor mask is one 16-byte load
@@ -773,8 +818,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                                                  st, limit, W_MREF));
             if (!alive) break;
             if (j > pc.t0) {
-              mpa = mref[(par ^ 1) * BM + ra];
-              mpb = mref[(par ^ 1) * BM + rb];
+              mpa = mref[(par ^ 1) * 64 + crow(ra)];
+              mpb = mref[(par ^ 1) * 64 + crow(rb)];
             }
           }
           // lazy rescale: move the reference max only when it grows by > 8 (log2);
@@ -790,8 +835,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
             mnb = mtb;
           }
           if (c == 0) {
-            mref[par * BM + ra] = mna;
-            mref[par * BM + rb] = mnb;
+            mref[par * 64 + crow(ra)] = mna;
+            mref[par * 64 + crow(rb)] = mnb;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(B_MREF + 4 * par + q));
@@ -809,7 +854,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
             const int afb = g & (kAfBufs - 1);
             const uint32_t afr = mapa(BAR(B_AF_FULL + afb), peer);
             if (c < 2)
-              st_async_u32(mapa(sbase + OFF_AF + (afb * BM + (c ? rb : ra)) * 4, peer),
+              st_async_u32(mapa(sbase + OFF_AF + (afb * 64 + crow(c ? rb : ra)) * 4, peer),
                            __float_as_uint(c ? alpha_b : alpha_a), afr);
           }
           const float nma = m_a == -INFINITY ? 0.f : -m_a, nmb = m_b == -INFINITY ? 0.f : -m_b;
@@ -832,18 +877,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           }
           pin(l_a);
           pin(l_b);
-          // P (single buffer) is free, and O stable, once P.V of tile g-1 completed in
-          // both CTAs (the (g-1)/2-th phase of the other parity's barrier)
-          if (g >= 1) {
-            alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + ((g - 1) & 1)), ((g - 1) >> 1) & 1, st,
+          // P tile g & 1 is free once P.V of tile g-2 completed in both CTAs (this
+          // parity's barrier, whose phases this warp observes in order)
+          const uint32_t pbuf = OFF_P + (g & 1) * kPBytes;
+          if (g >= 2) {
+            alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + (g & 1)), ((g - 2) >> 1) & 1, st,
                                                  limit, W_P_EMPTY));
             if (!alive) break;
           }
           // P rows ra, rb: the pair for keys 8k + 2c is 4 bytes at offset 4c of the
           // row's 16-byte chunk k, stored 128B-swizzled (chunk k of row r at k ^ (r & 7)).
           {
-            const uint32_t prow_a = sbase + OFF_P + ra * 128 + 4 * c;
-            const uint32_t prow_b = sbase + OFF_P + rb * 128 + 4 * c;
+            const uint32_t prow_a = sbase + pbuf + ra * 128 + 4 * c;
+            const uint32_t prow_b = sbase + pbuf + rb * 128 + 4 * c;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               asm volatile("st.shared.b32 [%0], %1;" :: "r"(prow_a + ((k ^ (ra & 7)) << 4)), "r"(pa[k]) : "memory");
@@ -854,9 +900,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           __syncwarp();
           if (lane == 0) {
             // our 16 rows of this quadrant are one contiguous 2 KiB block
-            const uint32_t off = OFF_P + own_base * 128;
+            const uint32_t off = pbuf + own_base * 128;
             bulk_copy_to_peer(mapa(sbase + off, peer), sbase + off, kPQuadBytes,
-                              mapa(BAR(B_P_RX), peer));
+                              mapa(BAR(B_P_RX + (g & 1)), peer));
           }
           // the peer's rescale factors for its rows of this quadrant: both halves of
           // O must carry the same reference maxima before P.V of this tile
@@ -865,10 +911,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                              wait<true>(BAR(B_AF_FULL + afb), (g / kAfBufs) & 1, st, limit, W_AF));
           if (!alive) break;
           next_af = g + 2;
-          const float qa = af[afb * BM + (ra ^ 16)], qb = af[afb * BM + (rb ^ 16)];
+          const float qa = af[afb * 64 + crow(ra)], qb = af[afb * 64 + crow(rb)];   // rows ra ^ 16, rb ^ 16
           if (warp == lead && lane == 0 && g + kAfBufs < G)
             mbar_expect_tx(BAR(B_AF_FULL + afb), kAfBytes);
           if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f || qa != 1.f || qb != 1.f)) {
+            // O is stable once P.V of tile g-1 completed in both CTAs.  The other
+            // parity's barrier cannot be a phase ahead of tile g-1 here (P.V of
+            // tile g+1 follows ours), nor behind it (P.V of tile g-2 completed).
+            if (g >= 1) {
+              alive = __all_sync(0xffffffffu, wait(BAR(B_P_EMPTY + ((g - 1) & 1)), ((g - 1) >> 1) & 1,
+                                                   st, limit, W_P_EMPTY));
+              if (!alive) break;
+            }
             tc_fence_after();
             rescale_o_rows(tmem + lane_own + kColO, alpha_a, alpha_b);
             rescale_o_rows(tmem + lane_peer + kColO, qa, qb);
@@ -876,7 +930,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
             tc_fence_before();
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(B_P_FULL));
+          if (lane == 0) mbar_arrive(BAR(B_P_FULL + (g & 1)));
         }
         if (!alive) break;
 
@@ -895,15 +949,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
             if (!alive) break;
           }
           if (c == 0) {
-            lpart[ra] = m_a; lpart[BM + ra] = l_a;
-            lpart[rb] = m_b; lpart[BM + rb] = l_b;
+            lpart[crow(ra)] = m_a; lpart[64 + crow(ra)] = l_a;
+            lpart[crow(rb)] = m_b; lpart[64 + crow(rb)] = l_b;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(B_LSUM));
         } else {
           alive = __all_sync(0xffffffffu, wait(BAR(B_LSUM), pi & 1, st, limit, W_LSUM));
           if (!alive) break;
-          const float m1a = lpart[ra], l1a = lpart[BM + ra], m1b = lpart[rb], l1b = lpart[BM + rb];
+          const float m1a = lpart[crow(ra)], l1a = lpart[64 + crow(ra)];
+          const float m1b = lpart[crow(rb)], l1b = lpart[64 + crow(rb)];
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(B_L_FREE));
           const float ma = fmaxf(m_a, m1a), mb = fmaxf(m_b, m1b);
