@@ -3,11 +3,9 @@
 // Validating a Native CUDA Speculative Decoding Engine", section "Input
 // Knowledge Required"):
 //
-//   absorb_tc_kernel            q_lat[r, h, :] = W_UK[h]^T q_nope[r, h, :]   (bf16 out)
-//   combine_uproj_small_kernel  o_lat = log-sum-exp merge of the split partials,
-//   combine_uproj_pipe_kernel   out[r, h, :] = W_UV[h] o_lat                 (fp32 out);
-//                               the first for batches whose grid fits one wave,
-//                               the second (K-chunk pipeline) for larger ones
+//   absorb_tc_kernel         q_lat[r, h, :] = W_UK[h]^T q_nope[r, h, :]   (bf16 out)
+//   combine_uproj_tc_kernel  o_lat = log-sum-exp merge of the split partials,
+//                            out[r, h, :] = W_UV[h] o_lat                 (fp32 out)
 //
 // Both run transposed so the weight matrix is the 128-row MMA operand and the
 // query rows are the MMA N dimension: D[128 x rows] = W-block . X^T, with the
@@ -127,235 +125,41 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   grid_dep_wait();
 }
 
-// ---- A5 + A6, small batches: the whole W_UV[h] in shared memory ------------------------
-// UP_NR query rows (b, i) per CTA: 16, 32 or 64, the smallest whose grid
-// (heads x row blocks) runs in one wave at one CTA per SM.  Shared memory: A = W_UV[h] as 8
-// chunks of 128 v-rows x 64 d; B = merged o_lat rows (bf16) as 8 chunks of
-// UP_NR rows x 64 d; per-row split weights; barriers.
-constexpr int UP_MAX_SPLITS = 64;
-constexpr int UP_OFF_B = 8 * 128 * 128;
-__host__ __device__ constexpr int up_off_w(int nr) { return UP_OFF_B + 8 * nr * 128; }
-__host__ __device__ constexpr int up_off_pr(int nr) { return up_off_w(nr) + nr * UP_MAX_SPLITS * 4; }
-__host__ __device__ constexpr int up1_off_bar(int nr) { return up_off_pr(nr) + nr * 16 + 16; }
-__host__ __device__ constexpr int up1_smem(int nr) { return up1_off_bar(nr) + 64 + 1024; }
-__host__ __device__ constexpr int up_tmem_cols(int nr) { return nr < 32 ? 32 : nr; }
-
-constexpr int UP_THREADS = 256;   // all warps merge partials
-constexpr int UP_BATCH = 4;       // row/8-column units merged per thread per pass
-
-template <int UP_NR>
-__global__ void __launch_bounds__(UP_THREADS, 1)
-combine_uproj_small_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) {
-  constexpr int UP_OFF_W = up_off_w(UP_NR), UP_OFF_PR = up_off_pr(UP_NR), UP_OFF_BAR = up1_off_bar(UP_NR);
-  constexpr int kCols = up_tmem_cols(UP_NR);
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(sm);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x;
-  const int r0 = blockIdx.y * UP_NR;
-  const int BNr = a.B * a.N;
-  const int nr = min(UP_NR, BNr - r0);
-  float* wts = reinterpret_cast<float*>(sm + UP_OFF_W);
-  // per row: partial row index of its partial s = pr_base[r] + s * pr_step[r]
-  long long* pr_base = reinterpret_cast<long long*>(sm + UP_OFF_PR);
-  int* pr_step = reinterpret_cast<int*>(sm + UP_OFF_PR + UP_NR * 8);
-  int* s_max = reinterpret_cast<int*>(sm + UP_OFF_PR + UP_NR * 12);
-  const uint32_t bar_full = sbase + UP_OFF_BAR, bar_mma = bar_full + 8;
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + UP_OFF_BAR + 16);
-
-  if (tid == 0) {
-    mbar_init(bar_full, 1);
-    mbar_init(bar_mma, 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) { tmem_alloc(sbase + UP_OFF_BAR + 16, kCols); tmem_relinquish(); }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  if (tid == 0) {   // W_UV[h]: 128 v-rows x 512 d, eight 64-column chunks
-    mbar_expect_tx(bar_full, 8 * 128 * 128);
-    for (int k = 0; k < 8; ++k)
-      tma_load_2d(sbase + k * 128 * 128, &tm_w, bar_full, 64 * k, h * 128);
-  }
-
-  grid_dep_wait();   // the split partials are written by the attention kernel
-
-  // Partial weights per row, with 1 / sum_s e^{m_s - m*} l_s folded in.  The
-  // UP_THREADS / UP_NR threads of a row (adjacent lanes) take every
-  // (UP_THREADS / UP_NR)-th partial and meet by shuffles, so the (m, l) loads
-  // of a row are in flight together.
-  constexpr int kTpr = UP_THREADS / UP_NR;
-  static_assert(kTpr >= 2 && kTpr <= 32 && (kTpr & (kTpr - 1)) == 0, "threads per row");
-  if (tid == 0) *s_max = 0;
-  for (int i = tid; i < UP_NR * UP_MAX_SPLITS; i += UP_THREADS) wts[i] = 0.f;
-  __syncthreads();
-  {
-    const int r = tid / kTpr, sub = tid % kTpr;
-    const bool live = r < nr;
-    const PartialRef pr = partials_of_row(a, (long long)(r0 + (live ? r : 0)) * a.H + h);
-    const int S = live ? (pr.count < UP_MAX_SPLITS ? pr.count : UP_MAX_SPLITS) : 0;
-    if (sub == 0) {
-      pr_base[r] = live ? pr.base : 0;
-      pr_step[r] = live ? (int)pr.step : 0;
-    }
-    constexpr int kPer = UP_MAX_SPLITS / kTpr;        // partials per thread at most
-    float2 ml[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int s = sub + k * kTpr;
-      ml[k] = s < S ? *reinterpret_cast<const float2*>(a.part_ml + (pr.base + (long long)s * pr.step) * 2)
-                    : make_float2(-INFINITY, 0.f);
-    }
-    float m = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k)
-      if (ml[k].y > 0.f) m = fmaxf(m, ml[k].x);
-#pragma unroll
-    for (int o = 1; o < kTpr; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float l = 0.f;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const float e = ml[k].y > 0.f ? expf(ml[k].x - m) : 0.f;
-      ml[k].x = e;
-      l += e * ml[k].y;
-    }
-#pragma unroll
-    for (int o = 1; o < kTpr; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    const float inv = l > 0.f ? a.o_scale / l : 0.f;
-    float* w = wts + r * UP_MAX_SPLITS;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int s = sub + k * kTpr;
-      if (s < S) w[s] = ml[k].x * inv;
-    }
-    if (live && sub == 0) atomicMax(s_max, S);
-  }
-  __syncthreads();
-  const int S = *s_max;
-
-  // o_lat rows -> bf16, 128-byte swizzled K-major operand: row r, 8-column unit u.
-  // Each pass merges UP_BATCH units per thread; the bf16 partials of up to four
-  // pieces are loaded per step, 4 x UP_BATCH x 16 bytes in flight per thread.
-  for (int base = tid; base < UP_NR * 64; base += UP_THREADS * UP_BATCH) {
-    float acc[UP_BATCH][8];
-#pragma unroll
-    for (int uu = 0; uu < UP_BATCH; ++uu)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[uu][e] = 0.f;
-    for (int s0 = 0; s0 < S; s0 += 4) {
-      uint4 x[4][UP_BATCH];
-      float ws[4][UP_BATCH];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int s = s0 + q;
-#pragma unroll
-        for (int uu = 0; uu < UP_BATCH; ++uu) {
-          const int idx = base + uu * UP_THREADS;
-          const int r = idx >> 6, u = idx & 63;
-          ws[q][uu] = (s < S && idx < UP_NR * 64 && r < nr) ? wts[r * UP_MAX_SPLITS + s] : 0.f;
-          x[q][uu] = ws[q][uu] != 0.f
-                         ? *reinterpret_cast<const uint4*>(
-                               a.part_o16 + (pr_base[r] + (long long)s * pr_step[r]) * 512 + 8 * u)
-                         : make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int uu = 0; uu < UP_BATCH; ++uu) {
-          const float w = ws[q][uu];
-          const uint32_t wv[4] = {x[q][uu].x, x[q][uu].y, x[q][uu].z, x[q][uu].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[uu][2 * j] = fmaf(w, __uint_as_float(wv[j] << 16), acc[uu][2 * j]);
-            acc[uu][2 * j + 1] = fmaf(w, __uint_as_float(wv[j] & 0xffff0000u), acc[uu][2 * j + 1]);
-          }
-        }
-    }
-#pragma unroll
-    for (int uu = 0; uu < UP_BATCH; ++uu) {
-      const int idx = base + uu * UP_THREADS;
-      if (idx >= UP_NR * 64) continue;
-      const int r = idx >> 6, u = idx & 63;
-      uint32_t pk[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) pk[j] = pack_bf16x2(acc[uu][2 * j], acc[uu][2 * j + 1]);
-      const uint32_t addr = sbase + UP_OFF_B + (u >> 3) * UP_NR * 128 + r * 128 +
-                            (((u & 7) ^ (r & 7)) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                   :: "r"(addr), "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]) : "memory");
-    }
-  }
-  fence_async_smem();
-  __syncthreads();
-
-  bool ok = true;
-  if (tid == 0) {
-    ok = wait(bar_full, 0, a.status, kLimitNs, 111);
-    if (ok) {
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, UP_NR, 0, 0);
-      for (int kk = 0; kk < 32; ++kk) {
-        uint64_t ad = smem_desc(sbase + (kk >> 2) * 128 * 128 + (kk & 3) * 32, 16, 1024);
-        uint64_t bd = smem_desc(sbase + UP_OFF_B + (kk >> 2) * UP_NR * 128 + (kk & 3) * 32, 16, 1024);
-        mma_bf16(tmem, ad, bd, idesc, kk > 0);
-      }
-    }
-    mma_commit(bar_mma);
-  }
-  __syncwarp();
-  ok = wait(bar_mma, 0, a.status, kLimitNs, 112) && ok;
-  ok = __all_sync(0xffffffffu, ok);
-  tc_fence_after();
-  if (ok && warp < 4) {
-    const int v = warp * 32 + lane;
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
-    for (int c0 = 0; c0 < UP_NR; c0 += 32) {
-      float x[32];
-      tmem_ld32(tmem + lane_addr + c0, x);   // columns past UP_NR (< kCols) are ignored
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int r = c0 + j;
-        if (r < nr) a.out[((long long)(r0 + r) * a.H + h) * 128 + v] = x[j];
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tmem, kCols); }
-}
-
-// ---- A5 + A6, large batches: W_UV[h] and o_lat streamed in K-chunks ---------------------
+// ---- A5 + A6: split combine fused with the W_UV up-projection ---------------------------
 // CTA (h, row block) computes out[r, h, :] for NR query rows r = (b, i) of
 // head h:  D[128 v x NR] (TMEM, fp32) = W_UV[h] (A: 128 v x 512 d, K-major)
 // . o_lat^T (B: NR rows x 512 d, K-major, bf16), over eight K-chunks of 64
-// latent columns.  Each chunk passes through one of kUpStages shared-memory
-// stages: TMA brings the chunk of W_UV[h] (16 KiB), all 256 threads merge
-// the rows' partials of those 64 columns (log-sum-exp weights) into the bf16
-// B tile, and one thread issues the chunk's four MMAs.  While the tensor core
-// runs chunk k the threads merge chunk k+1, and only 3 x (16 KiB + NR x
-// 128 B) of shared memory is held, so several CTAs share an SM and NR can
-// grow to 256 rows (one wave for large batches).
-constexpr int kUpStages = 3;
-constexpr int kUpChunks = 8;                  // 512 latent columns / 64
-constexpr int kUpABytes = 128 * 128;          // W_UV chunk: 128 v-rows x 64 d bf16
-__host__ __device__ constexpr int up_stage_bytes(int nr) { return kUpABytes + nr * 128; }
-__host__ __device__ constexpr int up_off_bar(int nr) { return kUpStages * up_stage_bytes(nr); }
-__host__ __device__ constexpr int up_smem(int nr) { return up_off_bar(nr) + 128 + 1024; }
+// latent columns; o_lat is the log-sum-exp merge of the row's piece
+// partials.  The merge is latency-bound (the partials come from L2 or DRAM),
+// so it runs in as few rounds of loads as registers allow: each round merges
+// CG chunks of kPB pieces at once, and the first round's loads are in flight
+// while the rows' (m, l) are read.  W_UV[h] sits in kAS shared-memory
+// stages: all eight chunks when the grid fits one CTA per SM, else a ring of
+// four, refilled from L2 (prefetched at the start) as the MMAs free them.
+constexpr int UP_THREADS = 256;    // all warps merge partials
+constexpr int kUpChunks = 8;       // 512 latent columns / 64
+constexpr int kUpABytes = 128 * 128;   // W_UV chunk: 128 v-rows x 64 d bf16
+__host__ __device__ constexpr int up_tpr(int nr) { return UP_THREADS / nr; }      // threads per row
+__host__ __device__ constexpr int up_units(int nr) { return 8 / up_tpr(nr); }     // 16-byte units per chunk
+__host__ __device__ constexpr int up_cg(int nr) {                                 // chunks per round
+  return up_units(nr) <= 2 ? 4 : up_units(nr) == 4 ? 2 : 1;
+}
+__host__ __device__ constexpr int up_pb(int nr) { return up_cg(nr) * up_units(nr) <= 4 ? 4 : 1; }
+__host__ __device__ constexpr int up_off_b(int as) { return as * kUpABytes; }
+__host__ __device__ constexpr int up_off_bar(int nr, int as) { return up_off_b(as) + up_cg(nr) * nr * 128; }
+__host__ __device__ constexpr int up_smem(int nr, int as) { return up_off_bar(nr, as) + 8 * 20 + 16 + 1024; }
+__host__ __device__ constexpr int up_tmem_cols(int nr) { return nr < 32 ? 32 : nr; }
 
-template <int NR>
-__global__ void __launch_bounds__(UP_THREADS, 2)
-combine_uproj_pipe_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) {
+template <int NR, int kAS>
+__global__ void __launch_bounds__(UP_THREADS, kAS == kUpChunks ? 1 : 2)
+combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) {
   static_assert(NR >= 32 && NR <= 256 && (NR & (NR - 1)) == 0, "rows per CTA");
-  constexpr int kTpr = UP_THREADS / NR;        // threads per row (1 .. 8)
-  constexpr int kUnits = 8 / kTpr;             // 16-byte units (8 columns) of a chunk per thread
-  constexpr int kPB = kUnits >= 2 ? 16 / kUnits : 8;   // pieces whose loads are in flight together
-  constexpr uint32_t kStage = up_stage_bytes(NR);
+  static_assert(kAS == kUpChunks || kAS == 4, "W_UV stages");
+  constexpr int kTpr = up_tpr(NR), kUnits = up_units(NR), CG = up_cg(NR), kPB = up_pb(NR);
+  constexpr int kRounds = kUpChunks / CG;
+  static_assert(kAS >= CG, "a round's W_UV chunks are resident together");
   constexpr int kCols = up_tmem_cols(NR);
+  constexpr int kOffB = up_off_b(kAS), kOffBar = up_off_bar(NR, kAS);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -365,123 +169,153 @@ combine_uproj_pipe_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a
   const int r0 = blockIdx.y * NR;
   const int BNr = a.B * a.N;
   const int nr = min(NR, BNr - r0);
-  auto A_FULL = [&](int s) -> uint32_t { return sbase + up_off_bar(NR) + 8u * s; };
-  auto EMPTY = [&](int s) -> uint32_t { return sbase + up_off_bar(NR) + 8u * (kUpStages + s); };
-  const uint32_t bar_done = sbase + up_off_bar(NR) + 8u * (2 * kUpStages);
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + up_off_bar(NR) + 64);
+  auto A_FULL = [&](int s) -> uint32_t { return sbase + kOffBar + 8u * s; };
+  auto A_EMPTY = [&](int s) -> uint32_t { return sbase + kOffBar + 8u * (kAS + s); };
+  const uint32_t bar_b = sbase + kOffBar + 8u * (2 * kAS);      // a round's MMAs read the B slots
+  const uint32_t bar_done = bar_b + 8u;
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + kOffBar + 8 * 20);
 
   if (tid == 0) {
-    for (int s = 0; s < kUpStages; ++s) {
+    for (int s = 0; s < kAS; ++s) {
       mbar_init(A_FULL(s), 1);
-      mbar_init(EMPTY(s), 1);
+      mbar_init(A_EMPTY(s), 1);
     }
+    mbar_init(bar_b, 1);
     mbar_init(bar_done, 1);
     fence_mbar_init();
   }
-  if (warp == 0) { tmem_alloc(sbase + up_off_bar(NR) + 64, kCols); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(sbase + kOffBar + 8 * 20, kCols); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  if (tid == 0)   // the first chunks of W_UV[h] do not depend on the attention kernel
-    for (int k = 0; k < kUpStages; ++k) {
+  if (tid == 0) {   // W_UV[h] does not depend on the attention kernel
+    for (int k = 0; k < kAS; ++k) {
       mbar_expect_tx(A_FULL(k), kUpABytes);
-      tma_load_2d(sbase + k * kStage, &tm_w, A_FULL(k), 64 * k, h * 128);
+      tma_load_2d(sbase + k * kUpABytes, &tm_w, A_FULL(k), 64 * k, h * 128);
     }
+    for (int k = kAS; k < kUpChunks; ++k) tma_prefetch_2d(&tm_w, 64 * k, h * 128);
+  }
 
   grid_dep_wait();   // the split partials are written by the attention kernel
 
-  // This thread's row and its partials: m* over the pieces that saw a key, and
-  // o_scale / l* folded into the weights.
   const int r = tid / kTpr, sub = tid % kTpr;
   const bool live = r < nr;
   const PartialRef pr = partials_of_row(a, (long long)(r0 + (live ? r : 0)) * a.H + h);
   const int S = live ? pr.count : 0;
+
+  // A round's loads: kPB pieces from s0, CG chunks from c0, this thread's units.
+  uint4 x[kPB][CG][kUnits];
+  float2 ml[kPB];
+  auto load = [&](int s0, int c0) {
+#pragma unroll
+    for (int q = 0; q < kPB; ++q) {
+      const int s = s0 + q;
+      const long long prow = pr.base + (long long)s * pr.step;
+      ml[q] = s < S ? *reinterpret_cast<const float2*>(a.part_ml + prow * 2) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int c = 0; c < CG; ++c)
+#pragma unroll
+        for (int uu = 0; uu < kUnits; ++uu)
+          x[q][c][uu] = s < S ? *reinterpret_cast<const uint4*>(a.part_o16 + prow * 512 + 64 * (c0 + c) +
+                                                                 8 * (sub * kUnits + uu))
+                              : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load(0, 0);   // in flight while the rows' (m, l) are read
+
+  // m* over the pieces that saw a key, and o_scale / l* (one pass, l follows
+  // the running max), eight loads in flight at a time
   float m = -INFINITY, l = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (pr.base + (long long)s * pr.step) * 2);
-    if (ml.y > 0.f) m = fmaxf(m, ml.x);
-  }
-  for (int s = 0; s < S; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (pr.base + (long long)s * pr.step) * 2);
-    if (ml.y > 0.f) l += expf(ml.x - m) * ml.y;
+  for (int t0 = 0; t0 < S; t0 += 8) {
+    float2 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      v[q] = t0 + q < S ? *reinterpret_cast<const float2*>(a.part_ml + (pr.base + (long long)(t0 + q) * pr.step) * 2)
+                        : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (v[q].y > 0.f) {
+        if (v[q].x > m) {
+          l = m == -INFINITY ? 0.f : l * expf(m - v[q].x);
+          m = v[q].x;
+        }
+        l += expf(v[q].x - m) * v[q].y;
+      }
   }
   const float inv = l > 0.f ? a.o_scale / l : 0.f;
 
   bool ok = true;
-  for (int kc = 0; kc < kUpChunks; ++kc) {
-    const int stg = kc % kUpStages;
-    const uint32_t st_a = sbase + stg * kStage, st_b = st_a + kUpABytes;
-    if (kc >= kUpStages) {
-      // the MMAs of chunk kc - kUpStages have read this stage
-      ok = wait(EMPTY(stg), ((kc / kUpStages) - 1) & 1, a.status, kLimitNs, 113) && ok;
-      if (tid == 0) {
-        mbar_expect_tx(A_FULL(stg), kUpABytes);
-        tma_load_2d(st_a, &tm_w, A_FULL(stg), 64 * kc, h * 128);
-      }
-    }
-    // Merge columns 64 kc + 8 u .. + 7 of row r for this thread's units u.
-    float acc[kUnits][8];
+  for (int g = 0; g < kRounds; ++g) {
+    const int c0 = g * CG;
+    float acc[CG][kUnits][8];
 #pragma unroll
-    for (int uu = 0; uu < kUnits; ++uu)
+    for (int c = 0; c < CG; ++c)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[uu][e] = 0.f;
-    for (int s0 = 0; s0 < S; s0 += kPB) {
-      uint4 x[kPB][kUnits];
-      float w[kPB];
+      for (int uu = 0; uu < kUnits; ++uu)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[c][uu][e] = 0.f;
+    for (int s0 = 0; s0 < S || s0 == 0; s0 += kPB) {
+      if (g > 0 || s0 > 0) load(s0, c0);
 #pragma unroll
       for (int q = 0; q < kPB; ++q) {
-        const int s = s0 + q;
-        w[q] = 0.f;
-        if (s < S) {
-          const long long prow = pr.base + (long long)s * pr.step;
-          const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + prow * 2);
-          w[q] = ml.y > 0.f ? expf(ml.x - m) * inv : 0.f;
-        }
+        const float w = ml[q].y > 0.f ? expf(ml[q].x - m) * inv : 0.f;   // 0 for a piece that saw no key
 #pragma unroll
-        for (int uu = 0; uu < kUnits; ++uu)
-          x[q][uu] = w[q] != 0.f
-                         ? *reinterpret_cast<const uint4*>(
-                               a.part_o16 + (pr.base + (long long)(s0 + q) * pr.step) * 512 + 64 * kc +
-                               8 * (sub * kUnits + uu))
-                         : make_uint4(0u, 0u, 0u, 0u);
-      }
+        for (int c = 0; c < CG; ++c)
 #pragma unroll
-      for (int q = 0; q < kPB; ++q)
+          for (int uu = 0; uu < kUnits; ++uu) {
+            const uint32_t wv[4] = {x[q][c][uu].x, x[q][c][uu].y, x[q][c][uu].z, x[q][c][uu].w};
 #pragma unroll
-        for (int uu = 0; uu < kUnits; ++uu) {
-          const uint32_t wv[4] = {x[q][uu].x, x[q][uu].y, x[q][uu].z, x[q][uu].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[uu][2 * j] = fmaf(w[q], __uint_as_float(wv[j] << 16), acc[uu][2 * j]);
-            acc[uu][2 * j + 1] = fmaf(w[q], __uint_as_float(wv[j] & 0xffff0000u), acc[uu][2 * j + 1]);
+            for (int j = 0; j < 4; ++j) {
+              acc[c][uu][2 * j] = fmaf(w, __uint_as_float(wv[j] << 16), acc[c][uu][2 * j]);
+              acc[c][uu][2 * j + 1] = fmaf(w, __uint_as_float(wv[j] & 0xffff0000u), acc[c][uu][2 * j + 1]);
+            }
           }
-        }
+      }
     }
-    // bf16 B tile, 128-byte swizzled K-major: row r, 16-byte unit u at (u ^ (r & 7))
+    // the B slots are rewritten: the previous round's MMAs must have read them
+    if (g > 0) ok = wait(bar_b, (g - 1) & 1, a.status, kLimitNs, 114) && ok;
+    // bf16 B slot c, 128-byte swizzled K-major: row r, 16-byte unit u at (u ^ (r & 7))
 #pragma unroll
-    for (int uu = 0; uu < kUnits; ++uu) {
-      const int u = sub * kUnits + uu;
-      uint32_t pk[4];
+    for (int c = 0; c < CG; ++c)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) pk[j] = pack_bf16x2(acc[uu][2 * j], acc[uu][2 * j + 1]);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
-                   :: "r"(st_b + r * 128 + (((u & 7) ^ (r & 7)) << 4)), "r"(pk[0]), "r"(pk[1]),
-                      "r"(pk[2]), "r"(pk[3]) : "memory");
-    }
+      for (int uu = 0; uu < kUnits; ++uu) {
+        const int u = sub * kUnits + uu;
+        uint32_t pk[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pk[j] = pack_bf16x2(acc[c][uu][2 * j], acc[c][uu][2 * j + 1]);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                     :: "r"(sbase + kOffB + c * NR * 128 + r * 128 + (((u & 7) ^ (r & 7)) << 4)),
+                        "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]) : "memory");
+      }
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
-      ok = wait(A_FULL(stg), (kc / kUpStages) & 1, a.status, kLimitNs, 111) && ok;
-      if (ok) {
-        tc_fence_after();
-        constexpr uint32_t idesc = idesc_bf16(128, NR, 0, 0);
+      constexpr uint32_t idesc = idesc_bf16(128, NR, 0, 0);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tmem, smem_desc(st_a + kk * 32, 16, 1024), smem_desc(st_b + kk * 32, 16, 1024),
-                   idesc, (kc > 0 || kk > 0));
+      for (int c = 0; c < CG; ++c) {
+        const int kc = c0 + c, stg = kc % kAS;
+        ok = wait(A_FULL(stg), (kc / kAS) & 1, a.status, kLimitNs, 111) && ok;
+        if (ok) {
+          tc_fence_after();
+          const uint32_t st_a = sbase + stg * kUpABytes, st_b = sbase + kOffB + c * NR * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem, smem_desc(st_a + kk * 32, 16, 1024), smem_desc(st_b + kk * 32, 16, 1024),
+                     idesc, (kc > 0 || kk > 0));
+        }
+        if (kAS < kUpChunks) mma_commit(A_EMPTY(stg));
       }
-      mma_commit(EMPTY(stg));
+      mma_commit(bar_b);
+      // refill the ring with the chunks kAS ahead once these MMAs have read it
+      if (kAS < kUpChunks)
+        for (int c = 0; c < CG; ++c) {
+          const int kc = c0 + c, nk = kc + kAS, stg = kc % kAS;
+          if (nk >= kUpChunks) continue;
+          ok = wait(A_EMPTY(stg), (kc / kAS) & 1, a.status, kLimitNs, 113) && ok;
+          mbar_expect_tx(A_FULL(stg), kUpABytes);
+          tma_load_2d(sbase + stg * kUpABytes, &tm_w, A_FULL(stg), 64 * nk, h * 128);
+        }
     }
   }
   if (tid == 0) mma_commit(bar_done);
@@ -496,14 +330,14 @@ combine_uproj_pipe_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a
   if (ok && c_beg < NR) {
     const int v = (warp & 3) * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    for (int c0 = c_beg; c0 < c_beg + kHalfCols; c0 += 32) {
-      float x[32];
-      tmem_ld32(tmem + lane_addr + c0, x);
+    for (int cc = c_beg; cc < c_beg + kHalfCols; cc += 32) {
+      float y[32];
+      tmem_ld32(tmem + lane_addr + cc, y);
       tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int rr = c0 + j;
-        if (rr < nr) a.out[((long long)(r0 + rr) * a.H + h) * 128 + v] = x[j];
+        const int rr = cc + j;
+        if (rr < nr) a.out[((long long)(r0 + rr) * a.H + h) * 128 + v] = y[j];
       }
     }
   }
@@ -539,40 +373,28 @@ cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st, bool after_plan) {
 }
 
 namespace {
-template <int NR>
-cudaError_t launch_combine_small(const CUtensorMap& tw, const Args& a, cudaStream_t st, bool pdl) {
-  cudaError_t e = cudaFuncSetAttribute(combine_uproj_small_kernel<NR>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, up1_smem(NR));
+template <int NR, int kAS>
+cudaError_t launch_combine(const CUtensorMap& tw, const Args& a, cudaStream_t st, bool pdl) {
+  constexpr int smem = up_smem(NR, kAS);
+  static_assert(smem <= 227 * 1024 && (kAS == kUpChunks || 2 * smem <= 226 * 1024), "shared memory");
+  cudaError_t e = cudaFuncSetAttribute(combine_uproj_tc_kernel<NR, kAS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const unsigned nblk = (unsigned)(((long long)a.B * a.N + NR - 1) / NR);
-  return launch_ex(combine_uproj_small_kernel<NR>, dim3(a.H, nblk), dim3(UP_THREADS), up1_smem(NR),
-                   st, pdl, tw, a);
-}
-
-template <int NR>
-cudaError_t launch_combine_pipe(const CUtensorMap& tw, const Args& a, cudaStream_t st, bool pdl) {
-  cudaError_t e = cudaFuncSetAttribute(combine_uproj_pipe_kernel<NR>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, up_smem(NR));
-  if (e != cudaSuccess) return e;
-  const unsigned nblk = (unsigned)(((long long)a.B * a.N + NR - 1) / NR);
-  return launch_ex(combine_uproj_pipe_kernel<NR>, dim3(a.H, nblk), dim3(UP_THREADS), up_smem(NR),
-                   st, pdl, tw, a);
+  return launch_ex(combine_uproj_tc_kernel<NR, kAS>, dim3(a.H, nblk), dim3(UP_THREADS), smem, st, pdl,
+                   tw, a);
 }
 }  // namespace
 
-// Which combine + up-projection kernel, and its rows per CTA.  Small batches
-// (the grid fits one wave at one CTA per SM with 16, 32 or 64 rows): the
-// kernel that holds all of W_UV[h] and merges every column of its rows in one
-// pass, with many loads in flight.  Larger ones: the K-chunk pipeline, two
-// CTAs per SM with 64 or 128 rows, or one with 256.  Returns rows per CTA,
-// negative for the small-batch kernel.
+// Rows per CTA of the combine + up-projection: the smallest of 32, 64, 128,
+// 256 whose grid (heads x row blocks) runs in one wave at two CTAs per SM.
+// Returns it negated when the grid also fits one CTA per SM: then all of
+// W_UV[h] stays in shared memory.
 int combine_uproj_choice(const Args& a, int sms) {
   const long long bn = (long long)a.B * a.N;
-  for (int nr = 16; nr <= 64; nr <<= 1)
-    if ((long long)a.H * ((bn + nr - 1) / nr) <= sms) return -nr;
-  for (int nr = 64; nr <= 128; nr <<= 1)
-    if ((long long)a.H * ((bn + nr - 1) / nr) <= 2ll * sms) return nr;
-  return 256;
+  int nr = 32;
+  while (nr < 256 && (long long)a.H * ((bn + nr - 1) / nr) > 2ll * sms) nr <<= 1;
+  return (long long)a.H * ((bn + nr - 1) / nr) <= sms ? -nr : nr;
 }
 
 cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t st,
@@ -585,12 +407,14 @@ cudaError_t launch_combine_uproj_tc(const Args& a, const Plan& p, cudaStream_t s
   // Overlap with the attention kernel's tail unless phase events split the call.
   const bool pdl = ev == nullptr;
   const int c = combine_uproj_choice(a, p.sms);
-  cudaError_t e = c == -16 ? launch_combine_small<16>(tw, a, st, pdl)
-                : c == -32 ? launch_combine_small<32>(tw, a, st, pdl)
-                : c == -64 ? launch_combine_small<64>(tw, a, st, pdl)
-                : c == 64  ? launch_combine_pipe<64>(tw, a, st, pdl)
-                : c == 128 ? launch_combine_pipe<128>(tw, a, st, pdl)
-                           : launch_combine_pipe<256>(tw, a, st, pdl);
+  cudaError_t e = c == -32  ? launch_combine<32, kUpChunks>(tw, a, st, pdl)
+                : c == -64  ? launch_combine<64, kUpChunks>(tw, a, st, pdl)
+                : c == -128 ? launch_combine<128, kUpChunks>(tw, a, st, pdl)
+                : c == -256 ? launch_combine<256, kUpChunks>(tw, a, st, pdl)
+                : c == 32   ? launch_combine<32, 4>(tw, a, st, pdl)
+                : c == 64   ? launch_combine<64, 4>(tw, a, st, pdl)
+                : c == 128  ? launch_combine<128, 4>(tw, a, st, pdl)
+                            : launch_combine<256, 4>(tw, a, st, pdl);
   if (ev) cudaEventRecord(ev[4], st);
   return e;
 }

@@ -249,10 +249,11 @@ def test_tc_attention_with_simt_projections(paged):
 
 @pytest.mark.parametrize("B,N", [(1, 16), (5, 40), (9, 100)])
 def test_combine_uproj_kernels(B, N):
-    """The three shapes of the combine + up-projection step: one pass with all
-    of W_UV[h] in shared memory (B N = 16), and the K-chunk pipeline with 64
-    rows (B N = 200, last row block ragged) and 256 rows per CTA (B N = 900,
-    last block ragged), every node against the oracle."""
+    """Three shapes of the combine + up-projection kernel: 32 rows per CTA with
+    all of W_UV[h] in shared memory (B N = 16, one ragged row block), and the
+    four-stage W_UV ring with 64 rows (B N = 200, last row block ragged) and
+    256 rows per CTA (B N = 900, last block ragged), every node against the
+    oracle."""
     wl = small(f"combine_{B}_{N}", B=B, N=N, prefix=("uniform", 40, 120))
     _skip_tc(TC, wl)
     got, st, _ = run(wl, flags=TC)
