@@ -317,6 +317,7 @@ __device__ __noinline__ void store_o_quadrant(uint32_t ta0, __nv_bfloat16* dst0,
   }
 }
 
+template <bool kPaged>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                const __grid_constant__ CUtensorMap tm_ckv,
@@ -420,6 +421,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_ckv, (int)rank * kHalf + c * CH, row);
         tma_prefetch_2d(&tm_krope, kRopeHalf * (int)rank, row);
       };
+      auto prefetch_row = [&](int row) {
+        for (int c = 0; c < 4; ++c) tma_prefetch_2d(&tm_ckv, (int)rank * kHalf + c * CH, row);
+        tma_prefetch_2d(&tm_krope, kRopeHalf * (int)rank, row);
+      };
       Piece pc;
       bool have = piece_first(a, cl, beg, end, W, pc);
       int g = 0, pi = 0, issued = 0, qr_issued = 0;
@@ -432,30 +437,70 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           tma_load_2d(sbase + OFF_QR, &tm_qrope, BAR(B_QR_FULL), kRopeHalf * (int)rank,
                       (int)((long long)pc.b * nrows + pc.rt * BM));
         }
-        for (int j = pc.t0 + kStages; j < pc.t0 + kStages + kPrefetch && j < pc.t1; ++j)
-          prefetch(pc.b, j * BN);
-        for (int j = pc.t0; j < pc.t1; ++j, ++g) {
-          const int stg = g % kStages, rs = g % kRopeSlots;
-          if (g >= kStages &&
-              !wait(BAR(B_KV_EMPTY + stg), ((g / kStages) - 1) & 1, st, limit, W_KV_EMPTY)) {
-            alive = false;
-            break;
+        if constexpr (kPaged) {
+          // Paged: the cache rows of the piece's next kAhead + 1 tiles (one
+          // page-table load each), shifted by one per tile, so that neither
+          // tile j's copies nor the L2 prefetch kAhead tiles ahead wait for a
+          // page-table load; the row kAhead + 1 ahead is loaded meanwhile.
+          constexpr int kAhead = kStages + kPrefetch;
+          int rows[kAhead + 2];
+#pragma unroll
+          for (int i = 0; i <= kAhead; ++i) rows[i] = pc.t0 + i < pc.t1 ? key_row(pc.b, (pc.t0 + i) * BN) : 0;
+          rows[kAhead + 1] = 0;
+#pragma unroll
+          for (int i = kStages; i < kAhead; ++i)
+            if (pc.t0 + i < pc.t1) prefetch_row(rows[i]);
+          for (int j = pc.t0; j < pc.t1; ++j, ++g) {
+            const int stg = g % kStages, rs = g % kRopeSlots;
+            if (j + kAhead + 1 < pc.t1) rows[kAhead + 1] = key_row(pc.b, (j + kAhead + 1) * BN);
+            if (g >= kStages &&
+                !wait(BAR(B_KV_EMPTY + stg), ((g / kStages) - 1) & 1, st, limit, W_KV_EMPTY)) {
+              alive = false;
+              break;
+            }
+            if (g >= kRopeSlots &&
+                !wait(BAR(B_R_EMPTY + rs), ((g / kRopeSlots) - 1) & 1, st, limit, W_KV_EMPTY)) {
+              alive = false;
+              break;
+            }
+            mbar_expect_tx(BAR(B_KV_FULL + stg), kStageBytes + kRopeChunk);
+            const uint32_t dst = sbase + OFF_KV + stg * kStageBytes;
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
+                          (int)rank * kHalf + c * CH, rows[0]);
+            tma_load_2d(sbase + OFF_ROPE + rs * kRopeChunk, &tm_krope, BAR(B_KV_FULL + stg),
+                        kRopeHalf * (int)rank, rows[0]);
+            issued = g + 1;
+            if (j + kAhead < pc.t1) prefetch_row(rows[kAhead]);
+#pragma unroll
+            for (int i = 0; i <= kAhead; ++i) rows[i] = rows[i + 1];
           }
-          if (g >= kRopeSlots &&
-              !wait(BAR(B_R_EMPTY + rs), ((g / kRopeSlots) - 1) & 1, st, limit, W_KV_EMPTY)) {
-            alive = false;
-            break;
+        } else {
+          for (int j = pc.t0 + kStages; j < pc.t0 + kStages + kPrefetch && j < pc.t1; ++j)
+            prefetch(pc.b, j * BN);
+          for (int j = pc.t0; j < pc.t1; ++j, ++g) {
+            const int stg = g % kStages, rs = g % kRopeSlots;
+            if (g >= kStages &&
+                !wait(BAR(B_KV_EMPTY + stg), ((g / kStages) - 1) & 1, st, limit, W_KV_EMPTY)) {
+              alive = false;
+              break;
+            }
+            if (g >= kRopeSlots &&
+                !wait(BAR(B_R_EMPTY + rs), ((g / kRopeSlots) - 1) & 1, st, limit, W_KV_EMPTY)) {
+              alive = false;
+              break;
+            }
+            const int row = key_row(pc.b, j * BN);
+            mbar_expect_tx(BAR(B_KV_FULL + stg), kStageBytes + kRopeChunk);
+            const uint32_t dst = sbase + OFF_KV + stg * kStageBytes;
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
+                          (int)rank * kHalf + c * CH, row);
+            tma_load_2d(sbase + OFF_ROPE + rs * kRopeChunk, &tm_krope, BAR(B_KV_FULL + stg),
+                        kRopeHalf * (int)rank, row);
+            issued = g + 1;
+            if (j + kStages + kPrefetch < pc.t1) prefetch(pc.b, (j + kStages + kPrefetch) * BN);
           }
-          const int row = key_row(pc.b, j * BN);
-          mbar_expect_tx(BAR(B_KV_FULL + stg), kStageBytes + kRopeChunk);
-          const uint32_t dst = sbase + OFF_KV + stg * kStageBytes;
-          for (int c = 0; c < 4; ++c)
-            tma_load_2d(dst + c * kKVChunk, &tm_ckv, BAR(B_KV_FULL + stg),
-                        (int)rank * kHalf + c * CH, row);
-          tma_load_2d(sbase + OFF_ROPE + rs * kRopeChunk, &tm_krope, BAR(B_KV_FULL + stg),
-                      kRopeHalf * (int)rank, row);
-          issued = g + 1;
-          if (j + kStages + kPrefetch < pc.t1) prefetch(pc.b, (j + kStages + kPrefetch) * BN);
         }
         ++pi;
         have = piece_next(a, end, W, pc);
@@ -1204,11 +1249,12 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
 
   TcCfg cfg;
   cfg.limit_ns = (a.flags & KDTV_FLAG_TEST_STALL) ? 20000000ull : 2000000000ull;
-  e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
+  // the paged cache reads its rows through the page table (its own producer loop)
+  const auto kern = a.page_size ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // Overlap with the absorb kernel's tail unless phase events split the call.
-  e = launch_ex(attn_tc_kernel, dim3((unsigned)(2 * a.sk_clusters)), dim3(kThreads), kSmemBytes,
+  e = launch_ex(kern, dim3((unsigned)(2 * a.sk_clusters)), dim3(kThreads), kSmemBytes,
                 st, /*pdl=*/ev == nullptr && !simt_proj, tqr, tck, tkr, a, cfg);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[2], st);
