@@ -85,12 +85,20 @@ int make_plan(const kdtv_dims* d, Plan* p) {
     if (p->sk_wmin < 1) p->sk_wmin = 1;
     p->sk_wforce = d->kv_chunk > 0 ? (d->kv_chunk + 63) / 64 : 0;
     long long clusters = sms / 2 > 0 ? sms / 2 : 1;
+    // The boundary-aware plan (a gap of kSkBoundary virtual units before each
+    // non-empty row tile but the first) where it measured faster: pairs
+    // whose ranges are short (the whole cache capacity under 128 key tiles
+    // per pair), and paged batches whose row tiles outnumber the pairs.
+    // Elsewhere (one long request; contiguous batches of a few thousand keys
+    // per request) the plain plan's kernel instance is as fast or faster.
+    p->sk_gap = (R * u_cap < 128 * clusters || (d->page_size && R > clusters)) ? kSkBoundary : 0;
+    const long long v_cap = R * u_cap + (long long)p->sk_gap * (R - 1);
     if (p->sk_wforce > 0) {
       const long long w = p->sk_wforce > p->sk_wmin ? p->sk_wforce : p->sk_wmin;
-      const long long need = (R * u_cap + w - 1) / w;
+      const long long need = (v_cap + w - 1) / w;
       if (need > clusters) clusters = need;
     }
-    if (clusters > (1 << 20) || R * u_cap >= (1ll << 30)) return KDTV_ERR_UNSUPPORTED;
+    if (clusters > (1 << 20) || v_cap >= (1ll << 30)) return KDTV_ERR_UNSUPPORTED;
     p->sk_clusters = (int)clusters;
     p->slots = (int)(R + clusters + 1);
     p->chunk = 64;
@@ -211,6 +219,7 @@ extern "C" int kdtv_verify_attn(const kdtv_dims* d, const void* q_nope, const vo
     a.sk_clusters = p.sk_clusters;
     a.sk_wmin = p.sk_wmin;
     a.sk_wforce = p.sk_wforce;
+    a.sk_gap = p.sk_gap;
   }
 
   cudaEvent_t* ev = d->phase_events;

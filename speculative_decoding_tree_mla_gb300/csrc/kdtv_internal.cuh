@@ -45,6 +45,7 @@ struct Plan {
   int sms;                // streaming multiprocessors of the current device
   // tensor-core path (stream-K): CTA pairs, W bounds, partial slots
   int sk_clusters, sk_wmin, sk_wforce, rt_count, slots;
+  int sk_gap;             // virtual units before each non-empty row tile but the first (0 or kSkBoundary)
   bool kv_widen;          // fp8 cache widened to bf16 copies at off_kvc / off_kvr
   size_t off_qlat, off_part_o, off_part_ml, off_olat, off_sk, off_anc, off_kvc, off_kvr, total;
 };
@@ -79,22 +80,32 @@ struct Args {
   float* part_ml;         // [splits, rows, 2] or [slots, 128, 2]  (running max m, sum l)
   float* o_lat;           // [rows, d_c]
   // Stream-K plan of the tensor-core attention (nullptr: split layout).
-  int* sk;                // kSkHeader ints {U, W, clusters, R}, then {S_r, u_r, base_r} per row tile,
-                          // then the row tile of each CTA pair's first unit, then (16-byte
-                          // aligned) 8 ints per pair: {r, S_r, u_r, base_r} of that tile, L_b
+  int* sk;                // kSkHeader ints {V, W, clusters, R}, then {vS_r, u_r, base_r} per row
+                          // tile (vS_r: the tile's start in the virtual sequence, see
+                          // sk_gap), then the row tile of each CTA pair's first piece, then
+                          // (16-byte aligned) 8 ints per pair: {r, vS_r, u_r, base_r} of that
+                          // tile, L_b, the pair's count of key tiles
   uint32_t* anc_g;        // [B, N, 4] ancestor masks, written by the plan kernel
   int rt_count;           // 128-row tiles per request
   int sk_clusters;        // CTA pairs launched
   int sk_wmin;            // lower bound on W (units per CTA pair)
   int sk_wforce;          // forced W from kv_chunk (0 = none)
+  int sk_gap;             // virtual units before each non-empty row tile but the first
 };
 
 constexpr int kSkHeader = 4;
+// Cost of a piece boundary in the stream-K schedule, in 64-key units (writing
+// one piece's partial and loading the next piece's Q cost about six tiles of
+// work).  With a gap of this many virtual units before every non-empty row
+// tile but the first, a CTA pair whose range crosses into another row tile
+// takes that many key tiles fewer.
+constexpr int kSkBoundary = 6;
 
 // Where the partials of query row `row` live: `count` partial rows at part
 // row index base + k * step (k = 0 .. count-1).  With a stream-K plan the
-// row's 128-row tile r was cut into pieces at multiples of W; its pieces hold
-// consecutive slots base_r .. base_r + count - 1.
+// row's 128-row tile r was cut into pieces at the multiples of W inside its
+// virtual range (vS_r, vS_r + u_r); its pieces hold consecutive slots
+// base_r .. base_r + count - 1.
 struct PartialRef {
   long long base, step;
   int count;
@@ -112,7 +123,7 @@ __device__ __forceinline__ PartialRef partials_of_row(const Args& a, long long r
   const int r = (rr / 128) * a.B + b, tr = rr % 128;   // lane-major row tiles
   const int W = a.sk[1];
   const int* e = a.sk + kSkHeader + 3 * r;
-  const int S = e[0], u = e[1], base = e[2];
+  const int S = e[0], u = e[1], base = e[2];   // S = vS_r
   p.count = u > 0 ? 1 + ((S + u + W - 1) / W - 1 - S / W) : 0;
   p.base = (long long)base * 128 + tr;
   p.step = 128;

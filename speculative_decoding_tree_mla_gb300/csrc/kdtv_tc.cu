@@ -221,6 +221,63 @@ __device__ bool piece_next(const Args& a, int end, int W, Piece& p) {
   return true;
 }
 
+// The same walk over the boundary-aware plan, whose virtual sequence has a
+// gap of sk_gap units before every non-empty row tile but the first: a
+// pair's range may begin in the gap before its first row tile, and may end
+// in the gap before the next.
+__device__ __forceinline__ void piece_fill_g(const Args& a, int r, int beg, int end, int W, Piece& p) {
+  const int* e = sk_row(a, r);
+  const int x0 = max(beg, e[0]);
+  p.r = r;
+  p.rt = r / a.B;
+  p.b = r - p.rt * a.B;
+  p.t0 = x0 - e[0];
+  p.t1 = min(end, e[0] + e[1]) - e[0];
+  p.slot = e[2] + (x0 / W - e[0] / W);   // the first piece of r starts at vS_r
+  p.L = a.prefix_len[p.b];
+}
+
+__device__ bool piece_first_g(const Args& a, int cl, int beg, int end, int W, Piece& p) {
+  if (beg >= end) return false;
+  const int R = a.B * a.rt_count;
+  const int4* rec = reinterpret_cast<const int4*>(a.sk + sk_rec_off(R, a.sk_clusters)) + 2 * cl;
+  const int4 v0 = rec[0], v1 = rec[1];
+  const int r = v0.x;
+  if (r < 0 || r >= R) return false;
+  const int x0 = max(beg, v0.y);
+  p.r = r;
+  p.rt = r / a.B;
+  p.b = r - p.rt * a.B;
+  p.t0 = x0 - v0.y;
+  p.t1 = min(end, v0.y + v0.z) - v0.y;
+  p.slot = v0.w + (x0 / W - v0.y / W);
+  p.L = v1.x;
+  return p.t0 < p.t1;
+}
+
+__device__ bool piece_next_g(const Args& a, int end, int W, Piece& p) {
+  const int R = a.sk[3];
+  const int u = sk_row(a, p.r)[0] + p.t1;
+  if (u >= end) return false;
+  int r = p.r + 1;
+  while (r < R && sk_row(a, r)[1] == 0) ++r;
+  if (r >= R || sk_row(a, r)[0] >= end) return false;
+  piece_fill_g(a, r, u, end, W, p);
+  return true;
+}
+
+template <bool kGap>
+__device__ __forceinline__ bool first_piece(const Args& a, int cl, int beg, int end, int W, Piece& p) {
+  if constexpr (kGap) return piece_first_g(a, cl, beg, end, W, p);
+  else return piece_first(a, cl, beg, end, W, p);
+}
+
+template <bool kGap>
+__device__ __forceinline__ bool next_piece(const Args& a, int end, int W, Piece& p) {
+  if constexpr (kGap) return piece_next_g(a, end, W, p);
+  else return piece_next(a, end, W, p);
+}
+
 // Keeps a value computed before the next wait: the compiler may otherwise
 // sink arithmetic whose result is only used after a wait below it, onto the
 // critical path that the wait ends.
@@ -317,7 +374,7 @@ __device__ __noinline__ void store_o_quadrant(uint32_t ta0, __nv_bfloat16* dst0,
   }
 }
 
-template <bool kPaged>
+template <bool kPaged, bool kGap>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                const __grid_constant__ CUtensorMap tm_ckv,
@@ -395,11 +452,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
   grid_dep_wait();
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const int nrows = a.N * a.H;
-  const int U = a.sk[0], W = a.sk[1];
+  const int U = a.sk[0], W = a.sk[1];              // U: the (virtual) length of the sequence
   const long long beg_ll = (long long)cl * W;
   const int beg = beg_ll < U ? (int)beg_ll : U;
   const int end = (long long)beg + W < U ? beg + W : U;
-  const int G = end - beg;                         // key tiles of this pair
+  // key tiles of this pair: its range, less the gaps of a boundary-aware plan
+  // (counted by the plan kernel)
+  int G;
+  if constexpr (kGap)
+    G = beg < end ? reinterpret_cast<const int4*>(a.sk + sk_rec_off(a.B * a.rt_count, a.sk_clusters))[2 * cl + 1].y
+                  : 0;
+  else
+    G = end - beg;
 
   if (warp == 0) {
     // ---- TMA producer --------------------------------------------------------------
@@ -426,7 +490,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         tma_prefetch_2d(&tm_krope, kRopeHalf * (int)rank, row);
       };
       Piece pc;
-      bool have = piece_first(a, cl, beg, end, W, pc);
+      bool have = first_piece<kGap>(a, cl, beg, end, W, pc);
       int g = 0, pi = 0, issued = 0, qr_issued = 0;
       bool alive = true;
       while (alive && have) {
@@ -503,7 +567,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
           }
         }
         ++pi;
-        have = piece_next(a, end, W, pc);
+        have = next_piece<kGap>(a, end, W, pc);
       }
       // Drain: every issued copy has landed before this CTA may exit.
       if (qr_issued >= 1) wait(BAR(B_QR_FULL), (qr_issued - 1) & 1, st, limit, W_DRAIN);
@@ -516,7 +580,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     if (lane == 0 && G > 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(BM, BN, 0, 0);
       Piece pc;
-      bool have = piece_first(a, cl, beg, end, W, pc);
+      bool have = first_piece<kGap>(a, cl, beg, end, W, pc);
       int g = 0, pi = 0;
       bool alive = true;
       while (alive && have) {
@@ -551,7 +615,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         mma_commit(BAR(B_Q_EMPTY));                 // Q (and q_rope) may be reloaded
         mma_commit(BAR(B_QR_EMPTY));
         ++pi;
-        have = piece_next(a, end, W, pc);
+        have = next_piece<kGap>(a, end, W, pc);
       }
       mma_commit(BAR(B_MMA_DONE));                 // drain every issued MMA (both issuers)
       wait(BAR(B_MMA_DONE), 0, st, limit, W_DRAIN);
@@ -562,7 +626,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     if (lane == 0 && G > 0) {
       constexpr uint32_t kIdescPV = idesc_bf16(BM, kHalf, 0, 1);
       Piece pc;
-      bool have = piece_first(a, cl, beg, end, W, pc);
+      bool have = first_piece<kGap>(a, cl, beg, end, W, pc);
       int g = 0, pi = 0;
       // phases of B_P_RX + b armed and consumed so far (both armed at set-up)
       int p_armed0 = 1, p_armed1 = G > 1 ? 1 : 0, p_used0 = 0, p_used1 = 0;
@@ -602,7 +666,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         if (!alive) break;
         // the piece's O is complete: tell the warps that write it out (those that
         // took the piece's last tile when another piece follows, else all)
-        have = piece_next(a, end, W, pc);
+        have = next_piece<kGap>(a, end, W, pc);
         if (!have || ((g - 1) & 1) == 0) mma_commit(BAR(B_O_FULL + 0));
         if (!have || ((g - 1) & 1) == 1) mma_commit(BAR(B_O_FULL + 1));
         ++pi;
@@ -630,7 +694,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
     const uint32_t lane32 = static_cast<uint32_t>(32 * q) << 16;
     bool alive = true;
     Piece pc;
-    bool have = piece_first(a, cl, beg, end, W, pc);
+    bool have = first_piece<kGap>(a, cl, beg, end, W, pc);
 
     if (!is_softmax) {
       // ---- sender: each piece's Q into TMEM; the peer's score rows -> its receive buffer --
@@ -718,7 +782,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
                          ((uint32_t)sha & 0xffffu) | ((uint32_t)shb << 16), rxfull_remote);
         }
         ++pi;
-        have = piece_next(a, end, W, pc);
+        have = next_piece<kGap>(a, end, W, pc);
       }
     } else {
       // ---- softmax of this CTA's rows ra = own_base + t/4, rb = ra + 8 ---------------
@@ -1030,7 +1094,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
         // B_O_FULL + par completes only for pieces that this parity writes, so
         // each warp sees its phases in order.
         Piece nx = pc;
-        have = piece_next(a, end, W, nx);
+        have = next_piece<kGap>(a, end, W, nx);
         if (!have ? !write_o(pc.slot, pc.rt, false, 128 * par, 4)
                   : (((g - 1) & 1) == par && !write_o(pc.slot, pc.rt, true, 0, 8))) {
           alive = false;
@@ -1063,13 +1127,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qrope,
 // ---- plan kernel ----------------------------------------------------------------------
 // CTA b < B: the ancestor masks of request b (and the tree check).  CTA B: the
 // stream-K plan.  Request b contributes rt_count row tiles of u_b = ceil((L_b
-// + N) / 64) key tiles each (0 if its prefix length is invalid); row tile r
-// starts at unit S_r of the whole sequence.  With U units in all, W =
-// max(ceil(U / clusters), wmin), or the forced W.  A row tile is cut where a
-// multiple of W falls inside it; its pieces take the consecutive partial slots
-// from base_r = r + floor(S_r / W) (base_{r+1} - base_r = 1 + the multiples of
-// W in (S_r, S_{r+1}], so the ranges never overlap).  The plan also lists, for
-// each CTA pair c, the row tile that holds its first unit c W.
+// + N) / 64) key tiles each (0 if its prefix length is invalid).  The units
+// are laid out in a virtual sequence in which every non-empty row tile but
+// the first is preceded by a gap of sk_gap units (0 when the host chose the
+// plain plan): row tile r starts at vS_r = S_r + sk_gap * (non-empty tiles
+// before r), and the sequence is V units long.  CTA pair c takes the virtual
+// range [cW, (c+1)W), W = max(ceil(V / clusters), wmin) (or the forced W); a
+// pair whose range crosses into another row tile spends part of it in a gap
+// and so takes fewer key tiles, which pays for the piece boundary.  A row
+// tile is cut where a multiple of W falls inside (vS_r, vS_r + u_r); its
+// pieces take consecutive partial slots from base_r (an exclusive scan of
+// the piece counts).  The plan also lists, for each pair, the row tile of
+// its first piece (the tile whose range, with the gap before it, holds cW),
+// with that tile's {vS_r, u_r, base_r}, the request's prefix length and the
+// pair's count of key tiles.
 __global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
   grid_dep_launch();   // the absorb kernel does not read the plan
   const int tid = threadIdx.x;
@@ -1085,13 +1156,15 @@ __global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
     }
     return;
   }
-  __shared__ int tmp[256];
-  __shared__ int carry;
+  __shared__ int tu[256], tn[256];
+  __shared__ int carry_u, carry_n;
   const int R = a.B * a.rt_count;
+  const int gap = a.sk_gap;
   int* e = a.sk + kSkHeader;
   const int cap = a.page_size ? a.max_pages * a.page_size : a.t_stride;
-  if (tid == 0) carry = 0;
+  if (tid == 0) carry_u = carry_n = 0;
   __syncthreads();
+  // units, virtual starts and (in e[3r+2], for now) the non-empty tiles before r
   for (int r0 = 0; r0 < R; r0 += 256) {
     const int r = r0 + tid;
     int u = 0;
@@ -1102,57 +1175,95 @@ __global__ void __launch_bounds__(256) sk_plan_kernel(const Args a) {
       if (!ok && r < a.B) record_error(a.status, KDTV_ERR_BAD_PREFIX, (unsigned)b);
       u = ok ? (L + a.N + BN - 1) / BN : 0;
     }
-    tmp[tid] = u;
+    tu[tid] = u;
+    tn[tid] = u > 0;
     __syncthreads();
-    for (int o = 1; o < 256; o <<= 1) {     // inclusive scan
-      const int x = tid >= o ? tmp[tid - o] : 0;
+    for (int o = 1; o < 256; o <<= 1) {     // inclusive scans
+      const int xu = tid >= o ? tu[tid - o] : 0, xn = tid >= o ? tn[tid - o] : 0;
       __syncthreads();
-      tmp[tid] += x;
+      tu[tid] += xu;
+      tn[tid] += xn;
       __syncthreads();
     }
     if (r < R) {
-      e[3 * r] = carry + tmp[tid] - u;
+      const int S = carry_u + tu[tid] - u, ne = carry_n + tn[tid] - (u > 0);
+      e[3 * r] = S + gap * ne;
       e[3 * r + 1] = u;
+      e[3 * r + 2] = ne;
     }
     __syncthreads();
-    if (tid == 255) carry += tmp[255];
+    if (tid == 255) { carry_u += tu[255]; carry_n += tn[255]; }
     __syncthreads();
   }
-  const int U = carry;
+  const int V = carry_u + gap * (carry_n > 1 ? carry_n - 1 : 0);
   int W;
   if (a.sk_wforce > 0) {
     W = a.sk_wforce > a.sk_wmin ? a.sk_wforce : a.sk_wmin;
   } else {
-    W = (U + a.sk_clusters - 1) / a.sk_clusters;
+    W = (V + a.sk_clusters - 1) / a.sk_clusters;
     if (W < a.sk_wmin) W = a.sk_wmin;
   }
   if (W < 1) W = 1;
-  // partial slots, and the row tile holding the first unit c W of each pair c
+  // each pair's first row tile and its count of key tiles
   int* first = e + 3 * R;
   const int npair = a.sk_clusters;
-  for (int c = tid; c < npair; c += 256) first[c] = R;
-  __syncthreads();
-  for (int r = tid; r < R; r += 256) {
-    const int S = e[3 * r], u = e[3 * r + 1];
-    e[3 * r + 2] = r + S / W;
-    const long long c_end = ((long long)S + u + W - 1) / W;
-    for (long long c = ((long long)S + W - 1) / W; c < c_end && c < npair; ++c) first[c] = r;
-  }
-  __syncthreads();
-  // per-pair first-piece records {r, S_r, u_r, base_r}, {L_b, 0, 0, 0}
   int4* rec = reinterpret_cast<int4*>(a.sk + sk_rec_off(R, npair));
   for (int c = tid; c < npair; c += 256) {
+    first[c] = R;
+    rec[2 * c + 1] = make_int4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += 256) {
+    const int vS = e[3 * r], u = e[3 * r + 1], ne = e[3 * r + 2];
+    if (u == 0) continue;
+    // pairs whose range starts in [vS - gap, vS + u) begin in this tile, if
+    // their range reaches it
+    const int claim = ne > 0 ? vS - gap : 0;
+    const long long c_end = ((long long)vS + u + W - 1) / W;
+    for (long long c = ((long long)claim + W - 1) / W; c < c_end && c < npair; ++c)
+      first[c] = (long long)vS < (c + 1) * W ? r : R;
+    for (long long c = vS / W; c < c_end && c < npair; ++c) {
+      const long long lo = c * W > vS ? c * W : vS;
+      const long long hi = (c + 1) * W < (long long)vS + u ? (c + 1) * W : (long long)vS + u;
+      atomicAdd(&rec[2 * c + 1].y, (int)(hi - lo));
+    }
+  }
+  __syncthreads();
+  // partial slots: base_r = the pieces of the row tiles before r
+  if (tid == 0) carry_u = 0;
+  __syncthreads();
+  for (int r0 = 0; r0 < R; r0 += 256) {
+    const int r = r0 + tid;
+    int cnt = 0;
+    if (r < R) {
+      const int vS = e[3 * r], u = e[3 * r + 1];
+      cnt = u > 0 ? 1 + ((vS + u + W - 1) / W - 1 - vS / W) : 0;
+    }
+    tu[tid] = cnt;
+    __syncthreads();
+    for (int o = 1; o < 256; o <<= 1) {
+      const int x = tid >= o ? tu[tid - o] : 0;
+      __syncthreads();
+      tu[tid] += x;
+      __syncthreads();
+    }
+    if (r < R) e[3 * r + 2] = carry_u + tu[tid] - cnt;
+    __syncthreads();
+    if (tid == 255) carry_u += tu[255];
+    __syncthreads();
+  }
+  // per-pair first-piece records {r, vS_r, u_r, base_r}, {L_b, key tiles, 0, 0}
+  for (int c = tid; c < npair; c += 256) {
     const int r = first[c];
-    int4 v0 = make_int4(r, 0, 0, 0), v1 = make_int4(0, 0, 0, 0);
+    int4 v0 = make_int4(r, 0, 0, 0);
     if (r < R) {
       v0.y = e[3 * r]; v0.z = e[3 * r + 1]; v0.w = e[3 * r + 2];
-      v1.x = a.prefix_len[r % a.B];
+      rec[2 * c + 1].x = a.prefix_len[r % a.B];
     }
     rec[2 * c] = v0;
-    rec[2 * c + 1] = v1;
   }
   if (tid == 0) {
-    a.sk[0] = U;
+    a.sk[0] = V;
     a.sk[1] = W;
     a.sk[2] = a.sk_clusters;
     a.sk[3] = R;
@@ -1249,8 +1360,10 @@ cudaError_t launch_tc(const Args& a, const Plan& p, cudaStream_t st, cudaEvent_t
 
   TcCfg cfg;
   cfg.limit_ns = (a.flags & KDTV_FLAG_TEST_STALL) ? 20000000ull : 2000000000ull;
-  // the paged cache reads its rows through the page table (its own producer loop)
-  const auto kern = a.page_size ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  // one instance per cache layout (the paged cache reads its rows through the
+  // page table: its own producer loop) and per plan (with or without gaps)
+  const auto kern = a.page_size ? (a.sk_gap ? attn_tc_kernel<true, true> : attn_tc_kernel<true, false>)
+                                : (a.sk_gap ? attn_tc_kernel<false, true> : attn_tc_kernel<false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // Overlap with the absorb kernel's tail unless phase events split the call.

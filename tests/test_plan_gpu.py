@@ -1,18 +1,25 @@
 """The device-built stream-K plan and ancestor masks, bit for bit.
 
 After a tensor-core call the workspace holds what `sk_plan_kernel` wrote:
-* the plan table: the header {U, W, pairs, R}; {S_r, u_r, base_r} per row tile
-  (row tiles lane-major, r = tile index * B + request); the row tile holding
-  each pair's first unit; one 8-int record per pair {r, S_r, u_r, base_r, L_b};
+* the plan table: the header {V, W, pairs, R}; {vS_r, u_r, base_r} per row
+  tile (row tiles lane-major, r = tile index * B + request; vS_r the tile's
+  start in the virtual sequence, which has a gap of 6 units before every
+  non-empty row tile but the first when the host chose the boundary-aware
+  plan, none otherwise); the row tile of each pair's first piece; one 8-int
+  record per pair {r, vS_r, u_r, base_r, L_b, key tiles};
 * the ancestor masks [B, N, 4] u32 (bit j of node i's mask set iff j lies on
   i's root path, i included).
 
 Both are integer results with one correct value, so they are compared exactly
-with a host model written from the same definitions: units per row tile
-ceil((L_b + N) / 64) (0 for an invalid prefix), W = max(ceil(U / pairs),
-ceil(u_cap / 62)), base_r = r + floor(S_r / W), and the root paths of
+with a host model written from the same definitions (the enumeration in
+tests/test_stream_k_plan.py checks that model against a walk of every pair's
+range): units per row tile ceil((L_b + N) / 64) (0 for an invalid prefix),
+the host's choice of gap, W = max(ceil(V / pairs), ceil(u_cap / 62)), base_r
+the exclusive scan of the tiles' piece counts, and the root paths of
 parent[].  The plan and the masks are the last two workspace regions of a
-bf16 tensor-core call, each 256-byte aligned.
+bf16 tensor-core call, each 256-byte aligned.  The cases cover both plans:
+"long_plain" (one request, 64 row tiles of 1026 units) and "batched" take
+the plain plan, the others the boundary-aware one.
 """
 
 import numpy as np
@@ -37,6 +44,7 @@ def a256(x):
 
 
 def host_plan(wl, pairs):
+    from tests.test_stream_k_plan import host_gap, plan, records
     s = wl.spec
     B, N, H = s.B, s.N, s.H
     rt = -(-(N * H) // 128)
@@ -46,23 +54,19 @@ def host_plan(wl, pairs):
     ok = (L >= 0) & (L + N <= t_cap)
     u_req = np.where(ok, -(-(L + N) // 64), 0)
     u = np.tile(u_req, rt)                      # r = tile index * B + request
-    S = np.concatenate([[0], np.cumsum(u)[:-1]])
-    U = int(u.sum())
-    wmin = max(1, -(-(-(-t_cap // 64)) // 62))
-    Wd = max(-(-U // pairs), wmin, 1)
-    base = np.arange(R) + S // Wd
-    first = np.full(pairs, R, dtype=np.int64)
-    for r in range(R):
-        for c in range(-(-int(S[r]) // Wd), min(-(-(int(S[r]) + int(u[r])) // Wd), pairs)):
-            first[c] = r
+    u_cap = -(-t_cap // 64)
+    wmin = max(1, -(-u_cap // 62))
+    p = plan(u, pairs, wmin, gap=host_gap(R, pairs, u_cap, paged=bool(wl.page_size)))
+    first, tiles = records(p, pairs)
     rec = np.zeros((pairs, 8), dtype=np.int64)
     for c in range(pairs):
         r = int(first[c])
         rec[c, 0] = r
         if r < R:
-            rec[c, 1:4] = S[r], u[r], base[r]
+            rec[c, 1:4] = p["vS"][r], u[r], p["base"][r]
             rec[c, 4] = L[r % B]
-    return dict(U=U, W=Wd, R=R, S=S, u=u, base=base, first=first, rec=rec)
+        rec[c, 5] = tiles[c]
+    return dict(V=p["V"], W=p["W"], R=R, vS=p["vS"], u=u, base=p["base"], first=first, rec=rec)
 
 
 def host_masks(parent):
@@ -85,6 +89,7 @@ CASES = {
                                          prefix=("loguniform", 40, 900))),
     "batched": lambda: W.make("batched"),
     "kimi_single": lambda: W.make("kimi_single"),
+    "long_plain": lambda: W.make(W.small_spec("plan_l", B=1, N=128, prefix=("fixed", 65536))),
 }
 
 
@@ -109,9 +114,9 @@ def test_device_plan_and_masks_match_host_model(case):
     off_anc = ws.size - a256(B * N * 16)
     off_sk = off_anc - a256(sk_ints * 4)
     sk = ws[off_sk: off_sk + sk_ints * 4].view(np.int32).astype(np.int64)
-    assert sk[:4].tolist() == [hp["U"], hp["W"], pairs, R]
+    assert sk[:4].tolist() == [hp["V"], hp["W"], pairs, R]
     e = sk[4: 4 + 3 * R].reshape(R, 3)
-    assert np.array_equal(e[:, 0], hp["S"]) and np.array_equal(e[:, 1], hp["u"])
+    assert np.array_equal(e[:, 0], hp["vS"]) and np.array_equal(e[:, 1], hp["u"])
     assert np.array_equal(e[:, 2], hp["base"])
     assert np.array_equal(sk[4 + 3 * R: 4 + 3 * R + pairs], hp["first"])
     rec_off = (4 + 3 * R + pairs + 3) & ~3
