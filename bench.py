@@ -43,10 +43,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "long": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 929099008 + 10783488),
-    "kimi_single": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 9601024 + 0),
-    "batched": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 109074432 + 12553216),
-    "paged": ("4976ac893fec7126f5341e80a42a424830bfde96105247cd59a839a988590193", 941420544 + 35295232),
+    "long": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 916382208 + 10808832),
+    "kimi_single": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 9601024 + 0),
+    "batched": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 105821952 + 12524032),
+    "paged": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 739318016 + 34291712),
 }
 
 
