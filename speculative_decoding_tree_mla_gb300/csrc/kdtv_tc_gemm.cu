@@ -131,8 +131,8 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 // . o_lat^T (B: NR rows x 512 d, K-major, bf16), over eight K-chunks of 64
 // latent columns; o_lat is the log-sum-exp merge of the row's piece
 // partials.  The merge is latency-bound (the partials come from L2 or DRAM),
-// so it runs in as few rounds of loads as registers allow: each round merges
-// CG chunks of kPB pieces at once, and the first round's loads are in flight
+// so it runs in as few passes of loads as registers allow: each pass merges
+// CG chunks of kPB pieces at once, and the first pass's loads are in flight
 // while the rows' (m, l) are read.  W_UV[h] sits in kAS shared-memory
 // stages: all eight chunks when the grid fits one CTA per SM, else a ring of
 // four, refilled from L2 (prefetched at the start) as the MMAs free them.
@@ -141,7 +141,7 @@ constexpr int kUpChunks = 8;       // 512 latent columns / 64
 constexpr int kUpABytes = 128 * 128;   // W_UV chunk: 128 v-rows x 64 d bf16
 __host__ __device__ constexpr int up_tpr(int nr) { return UP_THREADS / nr; }      // threads per row
 __host__ __device__ constexpr int up_units(int nr) { return 8 / up_tpr(nr); }     // 16-byte units per chunk
-__host__ __device__ constexpr int up_cg(int nr) {                                 // chunks per round
+__host__ __device__ constexpr int up_cg(int nr) {                                 // chunks per pass
   return up_units(nr) <= 2 ? 4 : up_units(nr) == 4 ? 2 : 1;
 }
 __host__ __device__ constexpr int up_pb(int nr) { return up_cg(nr) * up_units(nr) <= 4 ? 4 : 1; }
@@ -156,8 +156,8 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   static_assert(NR >= 32 && NR <= 256 && (NR & (NR - 1)) == 0, "rows per CTA");
   static_assert(kAS == kUpChunks || kAS == 4, "W_UV stages");
   constexpr int kTpr = up_tpr(NR), kUnits = up_units(NR), CG = up_cg(NR), kPB = up_pb(NR);
-  constexpr int kRounds = kUpChunks / CG;
-  static_assert(kAS >= CG, "a round's W_UV chunks are resident together");
+  constexpr int kPasses = kUpChunks / CG;
+  static_assert(kAS >= CG, "a pass's W_UV chunks are resident together");
   constexpr int kCols = up_tmem_cols(NR);
   constexpr int kOffB = up_off_b(kAS), kOffBar = up_off_bar(NR, kAS);
   extern __shared__ uint8_t smem_raw[];
@@ -171,7 +171,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   const int nr = min(NR, BNr - r0);
   auto A_FULL = [&](int s) -> uint32_t { return sbase + kOffBar + 8u * s; };
   auto A_EMPTY = [&](int s) -> uint32_t { return sbase + kOffBar + 8u * (kAS + s); };
-  const uint32_t bar_b = sbase + kOffBar + 8u * (2 * kAS);      // a round's MMAs read the B slots
+  const uint32_t bar_b = sbase + kOffBar + 8u * (2 * kAS);      // a pass's MMAs read the B slots
   const uint32_t bar_done = bar_b + 8u;
   volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + kOffBar + 8 * 20);
 
@@ -204,7 +204,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   const PartialRef pr = partials_of_row(a, (long long)(r0 + (live ? r : 0)) * a.H + h);
   const int S = live ? pr.count : 0;
 
-  // A round's loads: kPB pieces from s0, CG chunks from c0, this thread's units.
+  // A pass's loads: kPB pieces from s0, CG chunks from c0, this thread's units.
   uint4 x[kPB][CG][kUnits];
   float2 ml[kPB];
   auto load = [&](int s0, int c0) {
@@ -246,7 +246,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
   const float inv = l > 0.f ? a.o_scale / l : 0.f;
 
   bool ok = true;
-  for (int g = 0; g < kRounds; ++g) {
+  for (int g = 0; g < kPasses; ++g) {
     const int c0 = g * CG;
     float acc[CG][kUnits][8];
 #pragma unroll
@@ -273,7 +273,7 @@ combine_uproj_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const Args a) 
           }
       }
     }
-    // the B slots are rewritten: the previous round's MMAs must have read them
+    // the B slots are rewritten: the previous pass's MMAs must have read them
     if (g > 0) ok = wait(bar_b, (g - 1) & 1, a.status, kLimitNs, 114) && ok;
     // bf16 B slot c, 128-byte swizzled K-major: row r, 16-byte unit u at (u ^ (r & 7))
 #pragma unroll
