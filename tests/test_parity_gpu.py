@@ -261,6 +261,22 @@ def test_combine_uproj_kernels(B, N):
     check(wl, got, all_nodes(wl))
 
 
+def test_paged_plain_plan_instance():
+    """A paged batch with as many row tiles as fit the pairs (2 requests x 32
+    row tiles) and a capacity over 128 key tiles per pair takes the plain
+    stream-K plan on the paged instance of the attention kernel (the other
+    paged workloads take the boundary-aware plan).  Sampled nodes against the
+    oracle, and every output row against the CUDA-core fp32 path."""
+    wl = small("paged_plain", B=2, N=64, paged=True, prefix=("uniform", 9000, 12000))
+    _skip_tc(TC, wl)
+    got, st, _ = run(wl, flags=TC)
+    assert st == 0
+    check(wl, got, [(0, 0), (0, 63), (1, 17), (1, 40)])
+    ref, st2, _ = run(wl, flags=SIMT)
+    assert st2 == 0
+    assert per_row_rel(got, ref).max() <= ROW_REL
+
+
 # -- full-size workloads, every node ----------------------------------------------------
 FULL = ["kimi_single", "batched", "long", "paged"]
 _ORACLE = {}

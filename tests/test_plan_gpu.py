@@ -18,8 +18,9 @@ the host's choice of gap, W = max(ceil(V / pairs), ceil(u_cap / 62)), base_r
 the exclusive scan of the tiles' piece counts, and the root paths of
 parent[].  The plan and the masks are the last two workspace regions of a
 bf16 tensor-core call, each 256-byte aligned.  The cases cover both plans:
-"long_plain" (one request, 64 row tiles of 1026 units) and "batched" take
-the plain plan, the others the boundary-aware one.
+"long_plain" (one request, 64 row tiles of 1026 units), "paged_plain" (a
+paged batch of 64 row tiles, capacity 175 units each) and "batched" take the
+plain plan, the others the boundary-aware one.
 """
 
 import numpy as np
@@ -90,6 +91,8 @@ CASES = {
     "batched": lambda: W.make("batched"),
     "kimi_single": lambda: W.make("kimi_single"),
     "long_plain": lambda: W.make(W.small_spec("plan_l", B=1, N=128, prefix=("fixed", 65536))),
+    "paged_plain": lambda: W.make(W.small_spec("plan_pp", B=2, N=64, paged=True,
+                                               prefix=("uniform", 9000, 12000))),
 }
 
 
