@@ -156,6 +156,7 @@ int plan_status(const kdtv_dims* d, size_t* bytes) {
   if (bytes) *bytes = st == KDTV_OK ? p.total : 0;
   return st;
 }
+int device_sm_count() { return sm_count(); }
 }  // namespace kdtv
 
 extern "C" size_t kdtv_workspace_size(const kdtv_dims* d) {

@@ -241,6 +241,8 @@ int tc_supported(const kdtv_dims* d);
 // Status kdtv_verify_attn returns on the host for these dims, and the
 // workspace bytes they need (0 unless KDTV_OK).
 int plan_status(const kdtv_dims* d, size_t* bytes);
+// SMs of the current device (0 if it cannot be queried).
+int device_sm_count();
 int tc_launches(const kdtv_dims* d, int splits);
 
 }  // namespace kdtv

@@ -23,24 +23,35 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 128;
 constexpr uint64_t kLimitNs = 2000000000ull;
 
 // ---- A1: absorb -----------------------------------------------------------------------
-constexpr int AB_M = 128;                  // latent columns per CTA
-constexpr int AB_NR = 128;                 // query rows (b, i) per CTA
+// CTA (latent block, head h, row-block group z) computes the 128 x 128 tiles
+// q_lat[rows of block rb, h, d0 .. d0+127] for rb = z, z + G, z + 2G, ...: the
+// W_UK block is loaded once and the query blocks stream through two stages.
+// Per tile, one MMA chain D[128 rows x 128 d] (TMEM, two buffers) = q_nope
+// rows (A, K-major) . W_UK block (B, MN-major).  The epilogue warps round D
+// to bf16 into the stage the MMAs have just read (128-byte swizzled, the
+// output tensor map's layout) and one thread stores it with TMA, which writes
+// whole lines; the stage is then refilled with the tile two ahead.
+constexpr int AB_M = 128;                  // latent columns per tile
+constexpr int AB_NR = 128;                 // query rows (b, i) per tile
+constexpr int AB_THREADS = 160;            // warps 0-3: epilogue (TMEM lane quadrants); 4: TMA + MMA
+constexpr int AB_STAGE_OUT = 2 * AB_NR * 128;   // a bf16 output tile as two 64-column boxes
 
-// Shared memory of absorb_tc_kernel for a given d_nope: A = two MN atoms of
-// d_nope e-rows x 128 B, B = d_nope/64 chunks of AB_NR rows x 128 B, barriers.
-__host__ __device__ constexpr int ab_off_b(int d_nope) { return 2 * d_nope * 128; }
-__host__ __device__ constexpr int ab_off_bar(int d_nope) {
-  return ab_off_b(d_nope) + (d_nope / 64) * AB_NR * 128;
+// Shared memory of absorb_tc_kernel for a given d_nope: the W_UK block (two
+// MN atoms of d_nope e-rows x 128 B), two stages each holding a query block
+// (d_nope/64 chunks of AB_NR rows x 128 B) or an output tile, barriers.
+__host__ __device__ constexpr int ab_stage(int d_nope) {
+  return (d_nope / 64) * AB_NR * 128 > AB_STAGE_OUT ? (d_nope / 64) * AB_NR * 128 : AB_STAGE_OUT;
 }
+__host__ __device__ constexpr int ab_off_q(int d_nope) { return 2 * d_nope * 128; }
+__host__ __device__ constexpr int ab_off_bar(int d_nope) { return ab_off_q(d_nope) + 2 * ab_stage(d_nope); }
 __host__ __device__ constexpr int ab_smem(int d_nope) { return ab_off_bar(d_nope) + 64 + 1024; }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(AB_THREADS, 1)
 absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_q,
-                 const Args a) {
+                 const __grid_constant__ CUtensorMap tm_o, const Args a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -48,78 +59,119 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int d0 = blockIdx.x * AB_M;
   const int h = blockIdx.y;
-  const int r0 = blockIdx.z * AB_NR;
-  const int BNr = a.B * a.N;
-  const int nr = min(AB_NR, BNr - r0);
+  const int z = blockIdx.z, G = gridDim.z;
+  const int RB = (a.B * a.N + AB_NR - 1) / AB_NR;
+  const int nk = (RB - z + G - 1) / G;       // this CTA's tiles (z < RB)
   const int kch = a.d_nope / 64;             // 64-wide K chunks
-  const int off_b = ab_off_b(a.d_nope), off_bar = ab_off_bar(a.d_nope);
-  const uint32_t bar_full = sbase + off_bar, bar_mma = bar_full + 8;
-  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + off_bar + 16);
+  const int stage = ab_stage(a.d_nope), off_q = ab_off_q(a.d_nope), off_bar = ab_off_bar(a.d_nope);
+  // barriers: W landed; [2] query stage landed; [2] MMA chain done; [2] output tile stored
+  const uint32_t bar_w = sbase + off_bar;
+  auto BAR_Q = [&](int s) -> uint32_t { return bar_w + 8u * (1 + s); };
+  auto BAR_MMA = [&](int s) -> uint32_t { return bar_w + 8u * (3 + s); };
+  auto BAR_OUT = [&](int s) -> uint32_t { return bar_w + 8u * (5 + s); };
+  volatile uint32_t* tslot = reinterpret_cast<volatile uint32_t*>(sm + off_bar + 56);
   grid_dep_launch();   // the attention kernel may start its prologue early
 
   if (tid == 0) {
-    mbar_init(bar_full, 1);
-    mbar_init(bar_mma, 1);
+    for (int b = 0; b < 7; ++b) mbar_init(bar_w + 8u * b, 1);
     fence_mbar_init();
   }
-  if (warp == 0) { tmem_alloc(sbase + off_bar + 16, AB_NR); tmem_relinquish(); }
+  if (warp == 4) { tmem_alloc(sbase + off_bar + 56, 2 * AB_M); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  bool ok = true;
-  if (tid == 0) {
-    const uint32_t w_bytes = 2u * a.d_nope * 128u;
-    mbar_expect_tx(bar_full, w_bytes + kch * AB_NR * 128u);
-    for (int c = 0; c < 2; ++c)       // W_UK[h][:, d0 + 64c : +64]: e-rows x 64 d
-      tma_load_2d(sbase + c * a.d_nope * 128, &tm_w, bar_full, d0 + 64 * c, h * a.d_nope);
-    for (int k = 0; k < kch; ++k)     // q_nope rows r0.. of head h, e in [64k, 64k+64)
-      tma_load_2d(sbase + off_b + k * AB_NR * 128, &tm_q, bar_full, h * a.d_nope + 64 * k, r0);
-    ok = wait(bar_full, 0, a.status, kLimitNs, 101);
-    if (ok) {
-      tc_fence_after();
+  if (warp == 4) {
+    if (lane == 0) {
+      const uint32_t q_bytes = (uint32_t)kch * AB_NR * 128u;
+      auto load_q = [&](int k) {   // query block of tile k -> stage k & 1
+        const int s = k & 1;
+        mbar_expect_tx(BAR_Q(s), q_bytes);
+        for (int c = 0; c < kch; ++c)   // q_nope rows of head h, e in [64c, 64c+64)
+          tma_load_2d(sbase + off_q + s * stage + c * AB_NR * 128, &tm_q, BAR_Q(s),
+                      h * a.d_nope + 64 * c, (z + k * G) * AB_NR);
+      };
+      mbar_expect_tx(bar_w, 2u * a.d_nope * 128u);
+      for (int c = 0; c < 2; ++c)       // W_UK[h][:, d0 + 64c : +64]: e-rows x 64 d
+        tma_load_2d(sbase + c * a.d_nope * 128, &tm_w, bar_w, d0 + 64 * c, h * a.d_nope);
+      load_q(0);
+      if (nk > 1) load_q(1);
       // D[128 rows x 128 d] = q_nope rows (A, K-major) x W_UK block (B, MN-major);
       // rows past the last query row are zero-filled by TMA and never stored.
       const uint32_t idesc = idesc_bf16(AB_NR, AB_M, /*a_mn=*/0, /*b_mn=*/1);
-      for (int kk = 0; kk < a.d_nope / 16; ++kk) {
-        uint64_t ad = smem_desc(sbase + off_b + (kk >> 2) * AB_NR * 128 + (kk & 3) * 32, 16, 1024);
-        // B (MN-major): 64-column atoms a.d_nope*128 B apart, 8 e-rows per 1 KiB.
-        uint64_t bd = smem_desc(sbase + kk * 16 * 128, a.d_nope * 128, 1024);
-        mma_bf16(tmem, ad, bd, idesc, kk > 0);
+      bool ok = wait(bar_w, 0, a.status, kLimitNs, 101);
+      for (int k = 0; ok && k < nk; ++k) {
+        const int s = k & 1;
+        // stage s was refilled (and TMEM buffer s released) after tile k-2's store
+        if (!wait(BAR_Q(s), (k >> 1) & 1, a.status, kLimitNs, 102)) break;
+        tc_fence_after();
+        const uint32_t qs = sbase + off_q + s * stage;
+        for (int kk = 0; kk < a.d_nope / 16; ++kk) {
+          uint64_t ad = smem_desc(qs + (kk >> 2) * AB_NR * 128 + (kk & 3) * 32, 16, 1024);
+          // B (MN-major): 64-column atoms a.d_nope*128 B apart, 8 e-rows per 1 KiB.
+          uint64_t bd = smem_desc(sbase + kk * 16 * 128, a.d_nope * 128, 1024);
+          mma_bf16(tmem + AB_M * s, ad, bd, idesc, kk > 0);
+        }
+        mma_commit(BAR_MMA(s));
+        if (k + 2 < nk) {
+          ok = wait(BAR_OUT(s), (k >> 1) & 1, a.status, kLimitNs, 103);
+          if (ok) load_q(k + 2);
+        }
       }
     }
-    mma_commit(bar_mma);
-  }
-  __syncwarp();
-  ok = wait(bar_mma, 0, a.status, kLimitNs, 102) && ok;
-  ok = __all_sync(0xffffffffu, ok);
-  tc_fence_after();
-  if (ok && warp * 32 < nr) {
-    // TMEM lane = query row: each thread writes its row's 128 latent columns
-    // as sixteen 16-byte vectors.
+    __syncwarp();
+  } else {
+    // TMEM lane = the tile's row warp*32 + lane: its 128 latent columns go to
+    // row r of the two 64-column boxes, 16-byte chunk j at (j ^ (r & 7)) * 16.
     const int r = warp * 32 + lane;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.q_lat) +
-                                          ((long long)(r0 + (r < nr ? r : 0)) * a.H + h) * 512 + d0);
     const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    for (int k = 0; k < nk; ++k) {
+      const int s = k & 1;
+      // the four warps agree on going on (named barrier 1 with an AND), so none
+      // is left waiting at the barrier below after another gave up
+      const uint32_t got = wait(BAR_MMA(s), (k >> 1) & 1, a.status, kLimitNs, 104) ? 1u : 0u;
+      uint32_t all;
+      asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                   "barrier.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                   : "=r"(all) : "r"(got) : "memory");
+      if (!all) break;
+      tc_fence_after();
+      const uint32_t os = sbase + off_q + s * stage;
 #pragma unroll
-    for (int c = 0; c < AB_M / 32; ++c) {
-      float v[32];
-      tmem_ld32(tmem + lane_addr + 32 * c, v);
-      tmem_wait_ld();
-      if (r < nr) {
+      for (int c = 0; c < AB_M / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + lane_addr + AB_M * s + 32 * c, v);
+        tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[4 * c + q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
-                                      pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                      pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                                      pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        for (int q = 0; q < 4; ++q) {
+          const int J = 4 * c + q;       // 16-byte chunk of the row's 256 bytes
+          const uint32_t dst = os + (J >> 3) * AB_NR * 128 + r * 128 + ((J & 7) ^ (r & 7)) * 16;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                       :: "r"(dst), "r"(pack_bf16x2(v[8 * q], v[8 * q + 1])),
+                          "r"(pack_bf16x2(v[8 * q + 2], v[8 * q + 3])),
+                          "r"(pack_bf16x2(v[8 * q + 4], v[8 * q + 5])),
+                          "r"(pack_bf16x2(v[8 * q + 6], v[8 * q + 7])) : "memory");
+        }
       }
+      fence_async_smem();   // the tile's generic writes -> the TMA store's reads
+      tc_fence_before();
+      asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
+      if (tid == 0) {
+        const int x = h * 512 + d0, y = (z + k * G) * AB_NR;
+        tma_store_2d(&tm_o, os, x, y);
+        tma_store_2d(&tm_o, os + AB_NR * 128, x + 64, y);
+        bulk_commit();
+        bulk_wait_read_all();   // stage s and TMEM buffer s may be reused
+        mbar_arrive(BAR_OUT(s));
+      }
+      __syncwarp();
     }
+    if (tid == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tmem, AB_NR); }
+  if (warp == 4) { tc_fence_after(); tmem_dealloc(tmem, 2 * AB_M); }
   // Launched beside the attention plan: this grid completes only after the
   // plan has, so the attention kernel's wait on it covers both.
   grid_dep_wait();
@@ -359,17 +411,28 @@ bool combine_uproj_tc_ok(const Args& a) {
 
 cudaError_t launch_absorb_tc(const Args& a, cudaStream_t st, bool after_plan) {
   if (!absorb_tc_ok(a)) return launch_absorb(a, st, /*bf16_out=*/true);
-  CUtensorMap tw, tq;
+  if (reinterpret_cast<uintptr_t>(a.q_lat) & 15u) return cudaErrorMisalignedAddress;
+  CUtensorMap tw, tq, to;
   const uint64_t BNr = (uint64_t)a.B * a.N;
   if (encode_2d(&tw, a.W_UK, (uint64_t)a.H * a.d_nope, 512, 64, a.d_nope) != CUDA_SUCCESS ||
-      encode_2d(&tq, a.q_nope, BNr, (uint64_t)a.H * a.d_nope, 64, AB_NR) != CUDA_SUCCESS)
+      encode_2d(&tq, a.q_nope, BNr, (uint64_t)a.H * a.d_nope, 64, AB_NR) != CUDA_SUCCESS ||
+      encode_2d(&to, a.q_lat, BNr, (uint64_t)a.H * 512, 64, AB_NR) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const int smem = ab_smem(a.d_nope);
   cudaError_t e = cudaFuncSetAttribute(absorb_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(512 / AB_M, a.H, (unsigned)((BNr + AB_NR - 1) / AB_NR));
-  return launch_ex(absorb_tc_kernel, grid, dim3(kThreads), smem, st, after_plan, tw, tq, a);
+  // Row blocks per CTA: the (latent block, head) CTAs take every row block
+  // unless they leave most of one wave idle; then the row blocks are split
+  // into G groups.
+  const int rb = (int)((BNr + AB_NR - 1) / AB_NR);
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
+  const int per_sm = 228 * 1024 / (smem + 1024);
+  const long long ctas = 4ll * a.H;
+  int g = (int)((long long)sms * (per_sm > 0 ? per_sm : 1) / ctas);
+  g = g < 1 ? 1 : g > rb ? rb : g;
+  dim3 grid(512 / AB_M, a.H, (unsigned)g);
+  return launch_ex(absorb_tc_kernel, grid, dim3(AB_THREADS), smem, st, after_plan, tw, tq, to, a);
 }
 
 namespace {
