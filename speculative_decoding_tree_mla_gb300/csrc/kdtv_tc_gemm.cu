@@ -97,6 +97,9 @@ absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         tma_load_2d(sbase + c * a.d_nope * 128, &tm_w, bar_w, d0 + 64 * c, h * a.d_nope);
       load_q(0);
       if (nk > 1) load_q(1);
+      for (int k = 2; k < nk; ++k)      // later query blocks: into L2 now
+        for (int c = 0; c < kch; ++c)
+          tma_prefetch_2d(&tm_q, h * a.d_nope + 64 * c, (z + k * G) * AB_NR);
       // D[128 rows x 128 d] = q_nope rows (A, K-major) x W_UK block (B, MN-major);
       // rows past the last query row are zero-filled by TMA and never stored.
       const uint32_t idesc = idesc_bf16(AB_NR, AB_M, /*a_mn=*/0, /*b_mn=*/1);
