@@ -20,7 +20,8 @@ parent[].  The plan and the masks are the last two workspace regions of a
 bf16 tensor-core call, each 256-byte aligned.  The cases cover both plans:
 "long_plain" (one request, 64 row tiles of 1026 units), "paged_plain" (a
 paged batch of 64 row tiles, capacity 175 units each) and "batched" take the
-plain plan, the others the boundary-aware one.
+plain plan, the others the boundary-aware one; "many_tiles" (72 requests,
+1152 row tiles) runs the plan kernel's scans over several 256-tile rounds.
 """
 
 import numpy as np
@@ -93,6 +94,8 @@ CASES = {
     "long_plain": lambda: W.make(W.small_spec("plan_l", B=1, N=128, prefix=("fixed", 65536))),
     "paged_plain": lambda: W.make(W.small_spec("plan_pp", B=2, N=64, paged=True,
                                                prefix=("uniform", 9000, 12000))),
+    # 72 requests x 16 row tiles = 1152 row tiles: five rounds of the scans
+    "many_tiles": lambda: W.make(W.small_spec("plan_m", B=72, N=32, prefix=("uniform", 64, 256))),
 }
 
 
