@@ -7,10 +7,13 @@
 //   combine_uproj_tc_kernel  o_lat = log-sum-exp merge of the split partials,
 //                            out[r, h, :] = W_UV[h] o_lat                 (fp32 out)
 //
-// Both run transposed so the weight matrix is the 128-row MMA operand and the
-// query rows are the MMA N dimension: D[128 x rows] = W-block . X^T, with the
-// weight tile loaded by TMA (W_UK read as an MN-major operand) and the result
-// read back lane-per-output-feature, which makes the global writes coalesced.
+// The absorb takes the query rows as the 128-row MMA operand and the W_UK
+// block, loaded by TMA, as the MN-major N operand: D[128 rows x 128 d], read
+// back lane-per-row, rounded to bf16 in shared memory and stored by TMA.  The
+// combine runs transposed, so that W_UV[h] is the 128-row operand and the
+// query rows are the MMA N dimension: D[128 v x rows] = W_UV[h] . o_lat^T,
+// read back lane-per-output-feature, which makes its fp32 global writes
+// coalesced.
 
 #include <cuda.h>
 
