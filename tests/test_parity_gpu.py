@@ -233,6 +233,19 @@ def test_bf16_head_layouts(path, H, d_nope, d_v):
     check(wl, got, all_nodes(wl))
 
 
+@pytest.mark.parametrize("B,N,H", [(6, 48, 16), (5, 64, 32)])
+def test_absorb_row_block_groups(B, N, H):
+    """Few heads and several 128-row query blocks: the absorb kernel's
+    (latent block, head) CTAs would leave most of a wave idle, so it splits
+    the row blocks into groups (3 groups of one block for 16 heads; for 32
+    heads 2 groups, one CTA taking blocks 0 and 2, the other block 1)."""
+    wl = small(f"absorb_g_{H}", B=B, N=N, H=H, prefix=("uniform", 40, 600))
+    _skip_tc(TC, wl)
+    got, st, _ = run(wl, flags=TC)
+    assert st == 0
+    check(wl, got, all_nodes(wl))
+
+
 @pytest.mark.parametrize("paged", [False, True])
 def test_tc_attention_with_simt_projections(paged):
     """KDTV_FLAG_SIMT_PROJ: tensor-core attention between the CUDA-core absorb
