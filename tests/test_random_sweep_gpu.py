@@ -2,7 +2,8 @@
 from a seeded generator (batch, tree size and shape, head count, prefix
 lengths, contiguous or paged cache), each run on the tensor-core path (bf16
 bar) and the CUDA-core path (fp32 bar), every node of every request compared
-with the fp64 oracle.
+with the fp64 oracle; each with a bf16 cache and with an FP8 E4M3 cache (the
+oracle then reads the exactly dequantised values).
 
 The list spans what the hand-written cases pick one at a time: ragged
 batches of one to ten requests, 1 to 128 tree nodes, 4 to 64 heads (so the
@@ -51,11 +52,12 @@ def _configs(n=24, seed=2026):
 CONFIGS = _configs()
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8kv"])
 @pytest.mark.parametrize("path", ["tc", "simt"])
 @pytest.mark.parametrize("k", range(len(CONFIGS)))
-def test_random_config_every_node(k, path):
+def test_random_config_every_node(k, path, dtype):
     cfg = CONFIGS[k]
-    wl = W.make(W.small_spec(f"sweep_{k}", **cfg))
+    wl = W.make(W.small_spec(f"sweep_{k}", dtype=dtype, **cfg))
     flags = TC if path == "tc" else SIMT
     _skip_tc(flags, wl)
     got, st, _ = run(wl, flags=flags)
