@@ -43,10 +43,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "long": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 916382208 + 10808832),
-    "kimi_single": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 9601024 + 0),
-    "batched": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 105821952 + 12524032),
-    "paged": ("224e0990232bf98a229d4c82bf23fa675af4b63ef52dad87f12c3338b0f792ec", 739318016 + 34291712),
+    "long": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 920117760 + 10787328),
+    "kimi_single": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 9601024 + 0),
+    "batched": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 106299648 + 12567040),
+    "paged": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 708374272 + 33282560),
 }
 
 
