@@ -218,10 +218,11 @@ def test_bf16_edge_cases(path, case):
 
 @pytest.mark.parametrize("path", list(PATH_IDS))
 @pytest.mark.parametrize("H,d_nope,d_v", [(128, 128, 128), (16, 192, 128), (32, 64, 64),
-                                          (8, 96, 192)])
+                                          (8, 96, 192), (8, 256, 128)])
 def test_bf16_head_layouts(path, H, d_nope, d_v):
     """Head counts and head dims other than the Kimi layout, on the 512 + 64
-    latent cache: 128 heads (row tiles of one node), a 192-wide nope dim, and
+    latent cache: 128 heads (row tiles of one node), 192- and 256-wide nope
+    dims (the absorb's largest shared-memory layout, one CTA per SM), and
     head dims that the tensor-core absorb (d_nope % 64 != 0) or up-projection
     (d_v != 128) kernels do not take, so the call mixes tensor-core attention
     with CUDA-core projections."""
