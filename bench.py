@@ -43,10 +43,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture was taken on: a changed kernel reports null until it is captured
 # again.
 ATTN_TRAFFIC = {
-    "long": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 920117760 + 10787328),
-    "kimi_single": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 9601024 + 0),
-    "batched": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 106299648 + 12567040),
-    "paged": ("5d16ec5e6bf6e2d54d10c55cd3eac15e4ca55b9ac26bf2c88cc6fee1b766f13f", 708374272 + 33282560),
+    "long": ("b5d5562c0f989a7f2c3e99e4c95f34af435c9a3f864d73e4408a0c563882066b", 939578880 + 10908928),
+    "kimi_single": ("b5d5562c0f989a7f2c3e99e4c95f34af435c9a3f864d73e4408a0c563882066b", 9601024 + 0),
+    "batched": ("b5d5562c0f989a7f2c3e99e4c95f34af435c9a3f864d73e4408a0c563882066b", 109379328 + 12590080),
+    "paged": ("b5d5562c0f989a7f2c3e99e4c95f34af435c9a3f864d73e4408a0c563882066b", 710946048 + 33332224),
 }
 
 

@@ -7,19 +7,26 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 namespace kdtv {
 namespace {
 
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices];
+// SM count per device, cached on first use; host threads may race to fill an
+// entry (with the same value), hence atomics.
+std::atomic<int> g_sm_count[kMaxDevices];
 
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+  if (dev < kMaxDevices) {
+    const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < kMaxDevices) g_sm_count[dev] = n;
+  if (dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -68,6 +68,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "kdtv_internal.cuh"
 #include "kdtv_ptx.cuh"
 #include "kdtv_tmap.cuh"
@@ -1284,15 +1286,21 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Looked up on first use and cached; host threads may call concurrently (each
+// finds the same address), so the cache is an atomic.
+std::atomic<EncodeTiledFn> g_encoder{nullptr};
+
 EncodeTiledFn encoder() {
-  static EncodeTiledFn fn = nullptr;
+  EncodeTiledFn fn = g_encoder.load(std::memory_order_acquire);
   if (!fn) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<EncodeTiledFn>(p);
+      g_encoder.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }
