@@ -33,7 +33,8 @@
  *     its status_out argument; kdtv_get_device_status does not apply to it).
  *     The affected rows are left unwritten; nothing traps, and the CUDA
  *     context stays usable.
- *   - Calls that share a workspace must not overlap on the GPU.
+ *   - Calls that share a workspace must not overlap on the GPU.  Host threads
+ *     may call at the same time with separate workspaces.
  */
 #ifndef KDTV_H
 #define KDTV_H
